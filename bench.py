@@ -1,0 +1,433 @@
+"""Benchmark: exact attention forward on GB300 through the C-ABI.
+
+One step = the whole hot path on the headline workloads, inputs resident in
+device memory:
+  1. dense prefill, B1 H32 N8192 d128, non-causal        (fa_fwd)
+  2. the same, causal                                    (fa_fwd)
+  3. paged decode, B64 H32 d128, KV lengths U[512,16384],
+     16-token pages in a random permutation              (fa_paged_fwd)
+`value` is the prefill throughput in TFLOP/s (4 N^2 d per head, halved for
+causal) over legs 1-2; the decode leg is reported in GB/s of algorithmic
+bytes (every cached K/V byte once, plus q, o, lse and the block_table).
+L2 is flushed (256 MiB write) before every step; the decode pool (~8.9 GB)
+is far larger than L2 anyway.
+
+--impl reference times the float64 CPU oracle (a deliberately slow program)
+on a bounded sample of the same workload instead.
+
+For N > 1 (torchrun) each rank runs the same workload on its own GPU
+(replicas: the forward has no exchange step); timings are max-reduced and
+`value` counts the work of all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s & % BF16 peak (N=8192,d=128); paged-decode KV GB/s"
+C3 = dict(B=1, H=32, N=8192, d=128)
+C5 = dict(B=64, H=32, d=128)
+SEED_C3 = 1236
+SEED_C5 = 1239
+WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), then paged decode B64 H32 d128, "
+            "KV lengths uniform in [512,16384], 16-token pages in a seeded random permutation (fa_paged_fwd)")
+# DRAM bytes (read + write) of one non-causal prefill launch at the headline
+# size, from ncu (see profiles/prefill_kernel_B1H32N8192d128.txt); None when
+# the kernel changed after that capture.
+PREFILL_TRAFFIC_BYTES = None
+DECODE_TRAFFIC_BYTES = None
+
+
+def prefill_flops(N, d, H, B, causal):
+    f = 4.0 * N * N * d * H * B
+    return f / 2 if causal else f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------- oracle
+
+_C3_HOST = {}
+
+
+def run_cpu_oracle_sample(step: int, rows: int = 256):
+    """The float64 oracle on `rows` query rows of one head of the headline
+    prefill, non-causal and causal.  Returns (seconds, flops)."""
+    import numpy as np
+
+    import oracle
+    from exact_tiled_attention_fwd_gb300 import workloads as W
+
+    B, H, N, d = C3["B"], C3["H"], C3["N"], C3["d"]
+    if not _C3_HOST:
+        _C3_HOST["qkv"] = W.dense_inputs(B, N, H, d, SEED_C3, "cpu")
+    q, k, v = _C3_HOST["qkv"]
+    h = step % H
+    rng = np.random.default_rng(step)
+    sel = np.sort(rng.choice(N, size=rows, replace=False))
+    qh = q[0, sel, h].float().numpy().astype(np.float64)
+    kh = k[0, :, h].float().numpy().astype(np.float64)
+    vh = v[0, :, h].float().numpy().astype(np.float64)
+    scale = 1.0 / math.sqrt(d)
+    t0 = time.perf_counter()
+    oracle.attention_rows(qh, kh, vh, scale, False, rows=sel, Lq=N)
+    oracle.attention_rows(qh, kh, vh, scale, True, rows=sel, Lq=N)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * rows * N * d + 4.0 * float((sel + 1).sum()) * d
+    return dt, flops
+
+
+def cpu_baseline(budget_s: float = 20.0):
+    secs, flops, n = 0.0, 0.0, 0
+    while secs < budget_s and n < 2000:
+        dt, f = run_cpu_oracle_sample(n)
+        secs += dt
+        flops += f
+        n += 1
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} x 256 query rows of one head of the N=8192 d=128 prefill, non-causal and causal, "
+                      f"float64 numpy (BLAS default threads), {secs:.1f} s of CPU work"}
+
+
+def reference_arm(args, world, rank):
+    """--impl reference: the float64 oracle on the host cores."""
+    if rank != 0:
+        return
+    for s in range(args.warmup):
+        run_cpu_oracle_sample(10_000 + s)
+    secs, flops = 0.0, 0.0
+    for s in range(args.steps):
+        dt, f = run_cpu_oracle_sample(s)
+        secs += dt
+        flops += f
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "each step: 256 query rows of one head, non-causal + causal"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "256 query rows of one head of the N=8192 d=128 prefill per step, "
+                                   "non-causal and causal, float64 numpy"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- ours
+
+def ours(args, world, rank, local):
+    import torch
+
+    import exact_tiled_attention_fwd_gb300 as F
+    from exact_tiled_attention_fwd_gb300 import _build
+    from exact_tiled_attention_fwd_gb300 import workloads as W
+
+    _build.build()
+    F.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    B, H, N, d = C3["B"], C3["H"], C3["N"], C3["d"]
+    scale = 1.0 / math.sqrt(d)
+    do_prefill = args.case in ("all", "prefill")
+    do_decode = args.case in ("all", "decode")
+    q, k, v = W.dense_inputs(B, N, H, d, SEED_C3, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    lens = W.c5_lengths()[: args.decode_batch] if do_decode else [16]
+    pb = W.paged_inputs(lens, C5["H"], C5["d"], SEED_C5, dev, pool_on_device=True)
+    B5, H5, d5 = len(lens), C5["H"], C5["d"]
+    o5 = torch.empty_like(pb.q)
+    l5 = torch.empty((B5, H5), dtype=torch.float32, device=dev)
+    ws_bytes = F.fa_paged_workspace_size(B5, H5, d5, pb.max_seqlen)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    maxp = pb.block_table.shape[1]
+
+    def prefill(causal):
+        if not do_prefill:
+            return
+        st = F.fa_fwd(q, k, v, o, lse, B, H, H, N, d, scale, causal, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_fwd")
+
+    def decode():
+        if not do_decode:
+            return
+        st = F.fa_paged_fwd(pb.q, pb.k_cache, pb.v_cache, pb.block_table, pb.seqlens, o5, l5, B5, H5, H5, d5, 16,
+                            pb.num_pages, maxp, pb.max_seqlen, 1.0 / math.sqrt(d5), True, ws, ws_bytes, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_paged_fwd")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill(False)
+        prefill(True)
+        decode()
+    torch.cuda.synchronize()
+    st = F.fa_device_status(sp)
+    if st != F.FA_OK:
+        raise F.FAError(st, "warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.25)
+    wall0 = time.perf_counter()
+    for s in range(K):
+        flush.zero_()
+        e = ev[s]
+        e[0].record(stream)
+        prefill(False)
+        e[1].record(stream)
+        prefill(True)
+        e[2].record(stream)
+        decode()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop()
+    st = F.fa_device_status(sp)
+    if st != F.FA_OK:
+        raise F.FAError(st, "timed region")
+
+    t_nc = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    t_c = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    t_dec = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    t_nc, t_c, t_dec = (max_over_ranks(world, x) for x in (t_nc, t_c, t_dec))
+    f_nc = prefill_flops(N, d, H, B, False)
+    f_c = prefill_flops(N, d, H, B, True)
+    tflops = (f_nc + f_c) / ((t_nc + t_c) * 1e-3) / 1e12
+    kv_bytes = float(sum(lens)) * H5 * d5 * 2 * 2
+    dec_bytes = kv_bytes + 2 * B5 * H5 * d5 * 2 + B5 * H5 * 4 + sum((L + 15) // 16 for L in lens) * 4
+    gbs = dec_bytes / (t_dec * 1e-3) / 1e9
+    peak_tf, peak_gbs, peak_src = load_peaks()
+
+    if args.case != "all":
+        if rank == 0:
+            print(json.dumps({"case": args.case, "prefill_ms": [t_nc, t_c], "decode_ms": t_dec,
+                              "prefill_tflops": tflops if do_prefill else None,
+                              "decode_gbs": gbs if do_decode else None}), flush=True)
+        return
+
+    # ---- end to end through the public API with pinned host buffers
+    E = max(3, min(K, 30))
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    ho_c = torch.empty_like(ho).pin_memory()
+    hl_c = torch.empty_like(hl).pin_memory()
+    o_c = torch.empty_like(o)
+    lse_c = torch.empty_like(lse)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        st1 = F.fa_fwd(q, k, v, o, lse, B, H, H, N, d, scale, False, sp)
+        st2 = F.fa_fwd(q, k, v, o_c, lse_c, B, H, H, N, d, scale, True, sp)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        ho_c.copy_(o_c, non_blocking=True)
+        hl_c.copy_(lse_c, non_blocking=True)
+        if st1 or st2:
+            raise F.FAError(st1 or st2, "fa_fwd (e2e)")
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(world, e0.elapsed_time(e1) / E)
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = 2 * (o.numel() * o.element_size() + lse.numel() * lse.element_size())
+    e2e_tflops = (f_nc + f_c) / (t_e2e * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": tflops * world,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": t_nc + t_c + t_dec,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed by a 256 MiB write before every step; decode pool 8.9 GB > L2",
+                   "value_is": "prefill FLOPs / prefill time (legs 1-2), summed over ranks"},
+        "pct_bf16_peak": tflops / peak_tf,
+        "legs": {
+            "prefill_noncausal": {"ms": t_nc, "tflops": f_nc / (t_nc * 1e-3) / 1e12},
+            "prefill_causal": {"ms": t_c, "tflops": f_c / (t_c * 1e-3) / 1e12},
+            "paged_decode": {"ms": t_dec, "gbs": gbs, "frac_hbm": gbs / peak_gbs, "kv_tokens": int(sum(lens))},
+        },
+        "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": tflops, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": tflops / peak_tf, "traffic": PREFILL_TRAFFIC_BYTES,
+                     "peak_source": f"{peak_src} bf16 dense (burst)"},
+        "decode_roofline": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>", "bound": "hbm",
+                            "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                            "traffic": DECODE_TRAFFIC_BYTES, "peak_source": f"{peak_src} HBM copy"},
+        "e2e": {"value": e2e_tflops * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "what": "prefill legs with q,k,v copied from pinned host memory and O, LSE copied back each step"},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+        "wall_s_timed": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--case", choices=["all", "prefill", "decode"], default="all",
+                    help="run only one leg (for profiling); prints a short line instead of the bench line")
+    ap.add_argument("--decode-batch", type=int, default=64, help="sequences of the decode leg (profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        reference_arm(args, world, rank)
+        return
+    world, rank, local = dist_setup()
+    ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

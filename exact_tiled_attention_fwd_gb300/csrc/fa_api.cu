@@ -1,0 +1,303 @@
+// Host side of the C-ABI declared in include/fa.h: argument validation,
+// TMA descriptor encoding, kernel launches and the device error word.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+// Device error word: kernels OR FA_DEVERR_* bits into it.
+__device__ unsigned int g_fa_error_word;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+
+bool env_flag(const char* name) {
+    const char* v = std::getenv(name);
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+}
+
+unsigned long long wait_limit_ns() {
+    const char* v = std::getenv("FA_WAIT_LIMIT_NS");
+    if (v != nullptr && v[0] != '\0') {
+        const unsigned long long x = std::strtoull(v, nullptr, 10);
+        if (x > 0) return x;
+    }
+    return 2000000000ull;  // 2 s: far longer than any launch this library makes
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Resolve the driver entry point and this device's error-word address.
+fa_status ensure_init(unsigned int** err_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return FA_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (g_err_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_fa_error_word) != cudaSuccess) return FA_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<unsigned int*>(ptr);
+    }
+    *err_out = g_err_ptr[dev];
+    return FA_OK;
+}
+
+// 3-D view (d, heads, rows) of a [rows, heads, d] bf16 tensor; a box is 64
+// elements of d (128 bytes, the swizzle span) x 1 head x 128 rows.
+fa_status make_map(CUtensorMap* map, const void* base, int d, int heads, long long rows) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(fa::kBlockM)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status finish(cudaError_t e, cudaStream_t stream) {
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (env_flag("FA_CHECKED")) return static_cast<fa_status>(fa_device_status(stream, 1));
+    return FA_OK;
+}
+
+bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_abi_version(void) { return kAbiVersion; }
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID: return "FA_ERR_INVALID: bad argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: valid but not implemented";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait ran out";
+        case FA_ERR_DEVICE_INDEX: return "FA_ERR_DEVICE_INDEX: bad cu_seqlens/seqlens/block_table entry";
+        default: return "unknown fa_status";
+    }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+           float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o) return FA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID;
+    if (B < 1 || H < 1 || Hkv < 1 || N < 1 || H % Hkv != 0 || !scale_ok(scale)) return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const long long rows = static_cast<long long>(B) * N;
+    if (B > 65535 || H > 65535 || rows > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    CUtensorMap tq, tk, tv;
+    if ((st = make_map(&tq, q, d, H, rows)) != FA_OK) return st;
+    if ((st = make_map(&tk, k, d, Hkv, rows)) != FA_OK) return st;
+    if ((st = make_map(&tv, v, d, Hkv, rows)) != FA_OK) return st;
+    fa::PrefillParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.cu_q = nullptr;
+    p.cu_k = nullptr;
+    p.N = N;
+    p.num_seqs = B;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
+    p.max_seqlen_q = N;
+    p.max_seqlen_k = N;
+    p.total_q = static_cast<int>(rows);
+    p.total_k = static_cast<int>(rows);
+    p.num_q_blocks = (N + fa::kBlockM - 1) / fa::kBlockM;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.lse_head_stride = N;
+    p.err = err;
+    p.wait_limit_ns = wait_limit_ns();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
+}
+
+int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q,
+                  int total_k, int H, int Hkv, int d, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return FA_ERR_INVALID;
+    if (num_seqs < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 ||
+        max_seqlen_k < 1 || !scale_ok(scale))
+        return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    CUtensorMap tq, tk, tv;
+    if ((st = make_map(&tq, q, d, H, total_q)) != FA_OK) return st;
+    if ((st = make_map(&tk, k, d, Hkv, total_k)) != FA_OK) return st;
+    if ((st = make_map(&tv, v, d, Hkv, total_k)) != FA_OK) return st;
+    fa::PrefillParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.N = 0;
+    p.num_seqs = num_seqs;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
+    p.max_seqlen_q = max_seqlen_q;
+    p.max_seqlen_k = max_seqlen_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.num_q_blocks = (max_seqlen_q + fa::kBlockM - 1) / fa::kBlockM;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.lse_head_stride = total_q;
+    p.err = err;
+    p.wait_limit_ns = wait_limit_ns();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
+}
+
+size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen) {
+    if (B < 1 || H < 1 || max_seqlen < 0 || (d != 64 && d != 128)) return 0;
+    const size_t splits = static_cast<size_t>(fa::decode_max_splits(max_seqlen));
+    const size_t slots = static_cast<size_t>(B) * H * splits;
+    size_t bytes = slots * d * sizeof(float);
+    bytes = (bytes + 255) & ~size_t(255);
+    bytes += slots * 2 * sizeof(float);
+    return (bytes + 255) & ~size_t(255);
+}
+
+int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                 const int* seqlens, void* o, float* lse, int B, int H, int Hkv, int d, int page_size,
+                 int num_pages, int max_pages_per_seq, int max_seqlen, float scale, int causal, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+    (void)causal;  // a single newest-token query sees its whole cache either way
+    if (!q || !k_cache || !v_cache || !block_table || !seqlens || !o || !workspace) return FA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(workspace))
+        return FA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+        return FA_ERR_INVALID;
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || num_pages < 1 || max_pages_per_seq < 1 || max_seqlen < 0 ||
+        !scale_ok(scale))
+        return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (page_size != fa::kPageSize) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_pages_per_seq) * page_size < max_seqlen) return FA_ERR_INVALID;
+    if (B > 65535) return FA_ERR_UNSUPPORTED;
+    const size_t need = fa_paged_workspace_size(B, H, d, max_seqlen);
+    if (need == 0 || workspace_bytes < need) return FA_ERR_INVALID;
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    fa::DecodeParams p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_table = block_table;
+    p.seqlens = seqlens;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages_per_seq;
+    p.max_seqlen = max_seqlen;
+    p.split_tokens = fa::decode_split_tokens(max_seqlen);
+    p.max_splits = fa::decode_max_splits(max_seqlen);
+    const size_t slots = static_cast<size_t>(B) * H * p.max_splits;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((slots * d * sizeof(float) + 255) & ~size_t(255)));
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(fa::launch_decode(p, d, s), s);
+}
+
+int fa_paged_gather(const void* cache, const int* block_table, const int* seqlens, void* out, int B, int Hkv, int d,
+                    int page_size, int num_pages, int max_pages_per_seq, int max_seqlen, void* stream) {
+    if (!cache || !block_table || !seqlens || !out) return FA_ERR_INVALID;
+    if (!aligned16(cache) || !aligned16(out)) return FA_ERR_INVALID;
+    if (B < 1 || Hkv < 1 || num_pages < 1 || max_pages_per_seq < 1 || max_seqlen < 1) return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (page_size != fa::kPageSize || B > 65535) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_pages_per_seq) * page_size < max_seqlen) return FA_ERR_INVALID;
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    fa::GatherParams p{};
+    p.cache = cache;
+    p.block_table = block_table;
+    p.seqlens = seqlens;
+    p.out = out;
+    p.B = B;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages_per_seq;
+    p.max_seqlen = max_seqlen;
+    p.err = err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(fa::launch_gather(p, s), s);
+}
+
+int fa_device_status(void* stream, int clear) {
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    if (cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+    if (clear && word != 0) {
+        if (cudaMemsetAsync(err, 0, sizeof(unsigned int), s) != cudaSuccess) return FA_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (word & FA_DEVERR_TIMEOUT) return FA_ERR_TIMEOUT;
+    if (word & FA_DEVERR_INDEX) return FA_ERR_DEVICE_INDEX;
+    return FA_OK;
+}
+
+int fa_selftest_wait_timeout(long long limit_ns, void* stream) {
+    if (limit_ns <= 0 || limit_ns > 10000000000ll) return FA_ERR_INVALID;
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fa::launch_wait_selftest(err, static_cast<unsigned long long>(limit_ns), s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // extern "C"

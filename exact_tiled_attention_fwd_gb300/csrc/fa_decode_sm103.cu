@@ -1,0 +1,302 @@
+// Paged single-token decode for sm_103a: split-KV partial attention over the
+// page pool, then a combine of the per-split results.
+//
+// The cache is a pool of 16-token pages, [num_pages, 16, Hkv, d]; token t of
+// sequence b is page block_table[b][t / 16], slot t % 16 (the paged KV read
+// of the dlog.com.cn page "从标准 Attention 到 FlashAttention 与分页执行",
+// §3.4 and its PagedAttention section).  Decode reads every cached byte once,
+// so the kernel is bound by HBM bandwidth, not by arithmetic: no tensor cores.
+//
+// Split kernel: one warp per (sequence, head, split of split_tokens tokens).
+// A warp reads the split page by page with 16-byte loads; D/8 lanes hold one
+// key row (lane group g, element chunk c), so one warp instruction reads
+// 32/(D/8) whole rows, each a contiguous d*2-byte run.  Scores are the chunk
+// dot products summed across the row's lanes (xor shuffles); the running
+// (m, l, o) follow the online-softmax recurrence of the same page §2.2 with
+// the page as the block.  The split writes its unnormalised o and (m, l).
+//
+// Combine kernel: one warp per (sequence, head) merges the splits with the
+// same rescale rule: M = max m_s, w_s = 2^(m_s - M), l = sum w_s l_s,
+// O = sum w_s o_s / l, LSE = (M + log2 l) ln 2.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kDecodeWarps = 8;
+
+__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
+
+__device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr));
+    return r;
+}
+
+// Offset (in elements) of token `slot` of page `page`, kv head hk, element 0.
+__device__ __forceinline__ size_t paged_row_offset(int page, int slot, int Hkv, int hk, int d) {
+    return ((static_cast<size_t>(page) * kPageSize + slot) * Hkv + hk) * static_cast<size_t>(d);
+}
+
+// Page of logical token block `pg` of sequence b, or -1 (recorded as an index
+// error) when the table entry is outside the pool.
+__device__ __forceinline__ int lookup_page(const int* block_table, int max_pages, int num_pages, int b, int pg,
+                                           unsigned int* err) {
+    const int page = __ldg(block_table + static_cast<size_t>(b) * max_pages + pg);
+    if (static_cast<unsigned>(page) >= static_cast<unsigned>(num_pages)) {
+        atomicOr(err, FA_DEVERR_INDEX);
+        return -1;
+    }
+    return page;
+}
+
+__device__ __forceinline__ int clamp_seqlen(int L, int max_seqlen, unsigned int* err, bool report) {
+    if (L < 0 || L > max_seqlen) {
+        if (report) atomicOr(err, FA_DEVERR_INDEX);
+        return L < 0 ? 0 : max_seqlen;
+    }
+    return L;
+}
+
+__device__ __forceinline__ float dot8(const float (&q)[8], const uint4& k) {
+    float s = q[0] * bf16lo_to_f32(k.x);
+    s = fmaf(q[1], bf16hi_to_f32(k.x), s);
+    s = fmaf(q[2], bf16lo_to_f32(k.y), s);
+    s = fmaf(q[3], bf16hi_to_f32(k.y), s);
+    s = fmaf(q[4], bf16lo_to_f32(k.z), s);
+    s = fmaf(q[5], bf16hi_to_f32(k.z), s);
+    s = fmaf(q[6], bf16lo_to_f32(k.w), s);
+    s = fmaf(q[7], bf16hi_to_f32(k.w), s);
+    return s;
+}
+
+__device__ __forceinline__ void axpy8(float (&o)[8], float p, const uint4& v) {
+    o[0] = fmaf(p, bf16lo_to_f32(v.x), o[0]);
+    o[1] = fmaf(p, bf16hi_to_f32(v.x), o[1]);
+    o[2] = fmaf(p, bf16lo_to_f32(v.y), o[2]);
+    o[3] = fmaf(p, bf16hi_to_f32(v.y), o[3]);
+    o[4] = fmaf(p, bf16lo_to_f32(v.z), o[4]);
+    o[5] = fmaf(p, bf16hi_to_f32(v.z), o[5]);
+    o[6] = fmaf(p, bf16lo_to_f32(v.w), o[6]);
+    o[7] = fmaf(p, bf16hi_to_f32(v.w), o[7]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecodeWarps * 32) decode_split_kernel(const DecodeParams p) {
+    constexpr int LPR = D / 8;         // lanes per key row
+    constexpr int RPI = 32 / LPR;      // rows per warp load
+    constexpr int NI = kPageSize / RPI;  // loads per lane per page (K and V each)
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.z;
+    const int h = blockIdx.y * kDecodeWarps + warp;
+    const int split = blockIdx.x;
+    if (h >= p.H) return;
+    const int L = clamp_seqlen(__ldg(p.seqlens + b), p.max_seqlen, p.err, split == 0 && lane == 0);
+    const int t0 = split * p.split_tokens;
+    if (t0 >= L) return;
+    const int t1 = min(L, t0 + p.split_tokens);
+    const int hk = h / p.group;
+    const int g = lane / LPR;  // row group within a warp load
+    const int c = lane % LPR;  // 8-element chunk of the row
+
+    // q chunk, pre-multiplied by scale * log2(e) so scores are in log2 units
+    float qf[8];
+    {
+        const uint4 qv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                         (static_cast<size_t>(b) * p.H + h) * D + c * 8);
+        qf[0] = bf16lo_to_f32(qv.x) * p.scale_log2;
+        qf[1] = bf16hi_to_f32(qv.x) * p.scale_log2;
+        qf[2] = bf16lo_to_f32(qv.y) * p.scale_log2;
+        qf[3] = bf16hi_to_f32(qv.y) * p.scale_log2;
+        qf[4] = bf16lo_to_f32(qv.z) * p.scale_log2;
+        qf[5] = bf16hi_to_f32(qv.z) * p.scale_log2;
+        qf[6] = bf16lo_to_f32(qv.w) * p.scale_log2;
+        qf[7] = bf16hi_to_f32(qv.w) * p.scale_log2;
+    }
+    const uint16_t* kc = static_cast<const uint16_t*>(p.k_cache);
+    const uint16_t* vc = static_cast<const uint16_t*>(p.v_cache);
+    float m = neg_inf(), l = 0.f;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+
+    for (int pg = t0 / kPageSize; pg * kPageSize < t1; ++pg) {
+        const int page = lookup_page(p.block_table, p.max_pages, p.num_pages, b, pg, p.err);
+        if (page < 0) continue;
+        uint4 kv[NI], vv[NI];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const size_t off = paged_row_offset(page, i * RPI + g, p.Hkv, hk, D) + c * 8;
+            kv[i] = ldg_stream(kc + off);
+        }
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const size_t off = paged_row_offset(page, i * RPI + g, p.Hkv, hk, D) + c * 8;
+            vv[i] = ldg_stream(vc + off);
+        }
+        float s[NI];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) s[i] = dot8(qf, kv[i]);
+#pragma unroll
+        for (int off = LPR / 2; off >= 1; off >>= 1) {
+#pragma unroll
+            for (int i = 0; i < NI; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
+        }
+        float mp = neg_inf();
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int tok = pg * kPageSize + i * RPI + g;
+            if (tok >= t1) s[i] = neg_inf();
+            mp = fmaxf(mp, s[i]);
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, off));
+        const float m_new = fmaxf(m, mp);
+        const float mu = m_new == neg_inf() ? 0.f : m_new;
+        const float alpha = ex2(m - mu);  // m = -inf -> 0
+        l *= alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const float pi = ex2(s[i] - mu);
+            l += pi;
+            axpy8(acc, pi, vv[i]);
+        }
+        m = m_new;
+    }
+    // Sum the row groups: every lane of a group holds the same l; chunks add.
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
+        l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    }
+    const size_t slot = (static_cast<size_t>(b) * p.H + h) * p.max_splits + split;
+    if (g == 0) {
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D + c * 8);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    if (lane == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(m, l);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecodeWarps * 32) decode_combine_kernel(const DecodeParams p) {
+    constexpr int EPL = D / 32;  // elements per lane
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x * kDecodeWarps + warp;
+    if (bh >= p.B * p.H) return;
+    const int b = bh / p.H;
+    const int L = clamp_seqlen(__ldg(p.seqlens + b), p.max_seqlen, p.err, false);
+    const int ns = (L + p.split_tokens - 1) / p.split_tokens;
+    const size_t base = static_cast<size_t>(bh) * p.max_splits;
+    float M = neg_inf();
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, p.ws_ml[(base + s) * 2]);
+    const float mu = M == neg_inf() ? 0.f : M;
+    float l = 0.f;
+    float o[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+    for (int s = 0; s < ns; ++s) {
+        const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (base + s) * 2);
+        const float w = ex2(ml.x - mu);
+        l = fmaf(w, ml.y, l);
+        const float* src = p.ws_o + (base + s) * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, src[e], o[e]);
+    }
+    const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
+    uint16_t* dst = static_cast<uint16_t*>(p.o) + static_cast<size_t>(bh) * D + lane * EPL;
+    if constexpr (EPL == 4) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(o[0] * inv, o[1] * inv);
+    }
+    if (lane == 0 && p.lse != nullptr) {
+        float lg;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l));
+        p.lse[bh] = l > 0.f ? (M + lg) * kLn2 : neg_inf();
+    }
+}
+
+// Pure copy of every row the decode kernel would read, through the same
+// page lookup and row offset.  grid = (pages of the longest sequence, B).
+__global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
+    const int b = blockIdx.y;
+    const int pg = blockIdx.x;
+    const int L = clamp_seqlen(__ldg(p.seqlens + b), p.max_seqlen, p.err, pg == 0 && threadIdx.x == 0);
+    if (pg * kPageSize >= L) return;
+    const int page = lookup_page(p.block_table, p.max_pages, p.num_pages, b, pg, p.err);
+    if (page < 0) return;
+    const int chunks = p.d / 8;                    // 16-byte chunks per row
+    const int per_tok = p.Hkv * chunks;
+    const int ntok = min(kPageSize, L - pg * kPageSize);
+    const uint16_t* src = static_cast<const uint16_t*>(p.cache);
+    uint16_t* out = static_cast<uint16_t*>(p.out);
+    for (int u = threadIdx.x; u < ntok * per_tok; u += blockDim.x) {
+        const int slot = u / per_tok;
+        const int hk = (u % per_tok) / chunks;
+        const int cc = u % chunks;
+        const uint4 val = ldg_stream(src + paged_row_offset(page, slot, p.Hkv, hk, p.d) + cc * 8);
+        const size_t t = static_cast<size_t>(pg) * kPageSize + slot;
+        *reinterpret_cast<uint4*>(out + ((static_cast<size_t>(b) * p.max_seqlen + t) * p.Hkv + hk) * p.d + cc * 8) = val;
+    }
+}
+
+// One CTA waits on a barrier nothing arrives on; the bounded wait must give
+// up and record the timeout.
+__global__ void wait_selftest_kernel(unsigned int* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar_storage;
+    __shared__ int abort_flag;
+    const uint32_t bar = smem_u32(&bar_storage);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    mbar_wait(bar, 0, &abort_flag, err, limit_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream) {
+    dim3 grid(p.max_splits, (p.H + kDecodeWarps - 1) / kDecodeWarps, p.B);
+    dim3 cgrid((p.B * p.H + kDecodeWarps - 1) / kDecodeWarps);
+    if (d == 128) {
+        decode_split_kernel<128><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        decode_combine_kernel<128><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
+    } else {
+        decode_split_kernel<64><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        decode_combine_kernel<64><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
+    dim3 grid((p.max_seqlen + kPageSize - 1) / kPageSize, p.B);
+    gather_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,82 @@
+// Internal declarations shared by the host API (fa_api.cu) and the kernel
+// translation units.  Not part of the public ABI (that is include/fa.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+// Bits of the device error word.
+#define FA_DEVERR_TIMEOUT 1u
+#define FA_DEVERR_INDEX 2u
+
+namespace fa {
+
+// Query rows per tile, keys per K/V block of the prefill kernel.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+// Tokens per page of the paged KV cache.
+constexpr int kPageSize = 16;
+
+struct PrefillParams {
+    void* o;                 // bf16 [rows, H, d]
+    float* lse;              // fp32, may be null
+    const int* cu_q;         // varlen: int32 [num_seqs + 1]; null for dense
+    const int* cu_k;
+    int N;                   // dense: tokens per sequence (queries and keys)
+    int num_seqs;            // dense: B
+    int H, Hkv, group;       // group = H / Hkv
+    int max_seqlen_q, max_seqlen_k;
+    int total_q, total_k;    // rows of q/o and of k/v
+    int num_q_blocks;        // ceil(max_seqlen_q / kBlockM)
+    float scale_log2;        // scale * log2(e)
+    long long lse_head_stride;  // N (dense, [B,H,N]) or total_q (varlen, [H,total])
+    unsigned int* err;       // device error word
+    unsigned long long wait_limit_ns;
+};
+
+struct DecodeParams {
+    const void* q;           // bf16 [B, H, d]
+    const void* k_cache;     // bf16 [num_pages, page, Hkv, d]
+    const void* v_cache;
+    const int* block_table;  // int32 [B, max_pages]
+    const int* seqlens;      // int32 [B]
+    void* o;                 // bf16 [B, H, d]
+    float* lse;              // fp32 [B, H], may be null
+    float* ws_o;             // fp32 [B, H, max_splits, d] unnormalised partial O
+    float* ws_ml;            // fp32 [B, H, max_splits, 2] partial (m, l), log2 domain
+    int B, H, Hkv, group;
+    int num_pages, max_pages, max_seqlen;
+    int split_tokens;        // tokens per split (multiple of kPageSize)
+    int max_splits;
+    float scale_log2;
+    unsigned int* err;
+};
+
+struct GatherParams {
+    const void* cache;
+    const int* block_table;
+    const int* seqlens;
+    void* out;               // bf16 [B, max_seqlen, Hkv, d]
+    int B, Hkv, d;
+    int num_pages, max_pages, max_seqlen;
+    unsigned int* err;
+};
+
+// Kernel launchers (defined next to their kernels).
+cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int d, bool causal, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream);
+
+// Decode split sizing shared by the workspace query and the launch.
+inline int decode_split_tokens(int /*max_seqlen*/) { return 512; }
+inline int decode_max_splits(int max_seqlen) {
+    const int t = decode_split_tokens(max_seqlen);
+    const int s = (max_seqlen + t - 1) / t;
+    return s < 1 ? 1 : s;
+}
+
+}  // namespace fa

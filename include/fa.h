@@ -1,0 +1,168 @@
+/*
+ * Exact tiled attention forward for GB300 (sm_103a): the C-ABI.
+ *
+ * Every entry point computes, for each (sequence, head, query row i),
+ *
+ *     O_i   = sum_j softmax_j(scale * q_i . k_j) v_j
+ *     LSE_i = ln sum_j exp(scale * q_i . k_j)
+ *
+ * over the keys j visible to row i, without ever writing the score matrix S
+ * or the probability matrix P to device memory: Q is cut into row blocks,
+ * K/V are streamed in column blocks, and a running max m, running sum l and
+ * accumulator O are rescaled by exp(m_old - m_new) for every block, with O/l
+ * and m + ln l written at the end.  (Page "从标准 Attention 到 FlashAttention 与
+ * 分页执行", dlog.com.cn: opening definition, §2.1 tiling, §2.2 online
+ * softmax; page "L2.5 极致算子实战案例", yulong.wang: §2.1, O plus the per-row
+ * logsumexp is what the forward writes.)
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ *  - Tensors are bf16 (q, k, v, o, caches) or fp32 (lse), row-major, dense,
+ *    in DEVICE memory owned by the caller.  The library allocates nothing.
+ *    Every pointer must be 16-byte aligned.
+ *  - Accumulation is fp32; P is rounded to bf16 before the P.V product; O is
+ *    stored as bf16 round-to-nearest-even; LSE is the natural log, fp32.
+ *  - H is the number of query heads, Hkv the number of key/value heads,
+ *    H % Hkv == 0; query head h reads kv head h / (H / Hkv) (grouped-query
+ *    attention, the page's GQA section).  Hkv == H is plain multi-head.
+ *  - d (head dim) must be 64 or 128, else FA_ERR_UNSUPPORTED.
+ *  - scale multiplies q.k (callers pass 1/sqrt(d) for standard attention);
+ *    it must be finite and > 0, else FA_ERR_INVALID.
+ *  - causal = 1 masks with bottom-right alignment: key j is visible to query
+ *    i iff j <= i + (Lk - Lq).  For Lq == Lk this is the lower triangle with
+ *    the diagonal; a single decode query sees its whole cache.
+ *  - A query row with no visible key gets O = 0 and LSE = -inf.
+ *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Launches are asynchronous; no entry point synchronises unless the
+ *    environment variable FA_CHECKED=1 is set, in which case each call
+ *    synchronises its stream and returns the device-side status.
+ *  - Host-side validation runs before any launch and returns FA_ERR_INVALID
+ *    or FA_ERR_UNSUPPORTED without touching the GPU.  Index arrays that live
+ *    on the device (cu_seqlens, block_table, seqlens) are checked by the
+ *    kernels: a bad entry is skipped (its keys are treated as absent) and
+ *    recorded in a device error word that fa_device_status() reports.
+ *  - Every wait inside a kernel is bounded in time; on expiry the kernel
+ *    records FA_ERR_TIMEOUT in the device error word, drains its own copies,
+ *    frees its tensor memory and returns.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID = 1,      /* bad argument (null/unaligned pointer, size, scale) */
+    FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d not in {64,128}) */
+    FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    FA_ERR_TIMEOUT = 4,      /* a kernel wait ran out (device error word) */
+    FA_ERR_DEVICE_INDEX = 5  /* a kernel saw a bad cu_seqlens/block_table entry */
+} fa_status;
+
+/* Version of this ABI (bumped on any signature change). */
+int fa_abi_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char* fa_status_string(int status);
+
+/*
+ * Dense batched multi-head forward (the fixed-length interface of the
+ * dlog.com.cn page, §3.1).
+ *   q, o : [B, N, H, d]   bf16
+ *   k, v : [B, N, Hkv, d] bf16
+ *   lse  : [B, H, N]      fp32, may be NULL (then not written)
+ * Queries and keys have the same length N, so causal is the plain lower
+ * triangle.  B, N, H, Hkv >= 1.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int Hkv, int N, int d, float scale, int causal,
+           void* stream);
+
+/*
+ * Packed variable-length forward (the varlen interface of the dlog.com.cn
+ * page, §3.3): the tokens of num_seqs sequences are concatenated.
+ *   q, o : [total_q, H, d]   bf16
+ *   k, v : [total_k, Hkv, d] bf16
+ *   cu_seqlens_q, cu_seqlens_k : int32 [num_seqs + 1], DEVICE memory, prefix
+ *       sums of the per-sequence lengths (first 0, non-decreasing, last =
+ *       total).  Sequence s owns query rows [cu_q[s], cu_q[s+1]) and key rows
+ *       [cu_k[s], cu_k[s+1]); no row attends across sequences.  The two
+ *       arrays may be the same pointer.
+ *   max_seqlen_q, max_seqlen_k : upper bounds of the per-sequence lengths
+ *       (sizes the launch; a longer sequence is reported as
+ *       FA_ERR_DEVICE_INDEX and its excess rows are not computed).
+ *   lse  : [H, total_q] fp32, may be NULL.
+ */
+int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                  int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                  int H, int Hkv, int d, float scale, int causal, void* stream);
+
+/*
+ * Bytes of device workspace fa_paged_fwd needs for these sizes (the split-KV
+ * partial results).  Returns 0 for invalid sizes.
+ */
+size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen);
+
+/*
+ * Single-token decode over a paged KV cache (the kv-cache interface of the
+ * dlog.com.cn page, §3.4 and its PagedAttention section).
+ *   q, o      : [B, H, d] bf16 (one new token per sequence)
+ *   k_cache, v_cache : [num_pages, page_size, Hkv, d] bf16, the whole pool
+ *   block_table : int32 [B, max_pages_per_seq], DEVICE; logical token t of
+ *       sequence b is page block_table[b][t / page_size], slot
+ *       t % page_size.  Entries past ceil(seqlens[b] / page_size) are never
+ *       read.  An entry outside [0, num_pages) is skipped and reported as
+ *       FA_ERR_DEVICE_INDEX.
+ *   seqlens   : int32 [B], DEVICE; cached tokens per sequence, each in
+ *       [0, max_seqlen] (0 gives O = 0, LSE = -inf).
+ *   lse       : [B, H] fp32, may be NULL.
+ *   workspace : DEVICE scratch of at least
+ *       fa_paged_workspace_size(B, H, d, max_seqlen) bytes, 16-byte aligned;
+ *       it need not be initialised.
+ * page_size must be 16.  causal is accepted; under bottom-right alignment it
+ * does not change a single newest-token query.
+ */
+int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
+                 const int* block_table, const int* seqlens, void* o, float* lse,
+                 int B, int H, int Hkv, int d, int page_size, int num_pages,
+                 int max_pages_per_seq, int max_seqlen, float scale, int causal,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Copy, through the decode kernels' own page walk, the cached rows every
+ * sequence would read: out[b][t][hk][:] = cache[block_table[b][t/16]][t%16][hk][:]
+ * for t < seqlens[b].  out is bf16 [B, max_seqlen, Hkv, d] in DEVICE memory;
+ * rows t >= seqlens[b] are left untouched.  A test and debugging aid for the
+ * gather (a pure copy, so it must be bit-exact).
+ */
+int fa_paged_gather(const void* cache, const int* block_table, const int* seqlens, void* out,
+                    int B, int Hkv, int d, int page_size, int num_pages,
+                    int max_pages_per_seq, int max_seqlen, void* stream);
+
+/*
+ * Synchronise the stream, read the device error word and return FA_OK,
+ * FA_ERR_TIMEOUT or FA_ERR_DEVICE_INDEX (or FA_ERR_CUDA if the sync itself
+ * failed).  clear != 0 resets the word afterwards.
+ */
+int fa_device_status(void* stream, int clear);
+
+/*
+ * Self-test of the bounded wait: launch one CTA that waits on a barrier no
+ * one arrives on, with a limit of limit_ns nanoseconds.  The kernel must
+ * give up, record FA_ERR_TIMEOUT in the device error word and return, so the
+ * next fa_device_status() reports FA_ERR_TIMEOUT and the context stays
+ * usable.  No counterpart on the pages: it exists to test the failure path
+ * without faulting or hanging a GPU.
+ */
+int fa_selftest_wait_timeout(long long limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

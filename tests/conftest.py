@@ -11,3 +11,6 @@ if TESTS not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+from gpu_helpers import fa  # noqa: E402,F401  (session fixture for the GPU tests)

@@ -1,0 +1,93 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every function
+include/fa.h declares, and refuses bad arguments before touching a GPU."""
+
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_tiled_attention_fwd_gb300 import _build
+    import exact_tiled_attention_fwd_gb300 as F
+
+    _build.build()
+    F.load()
+    return F
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("fa_fwd", "fa_varlen_fwd", "fa_paged_fwd", "fa_paged_workspace_size", "fa_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    handle = lib.load()
+    missing = [n for n in declared_functions() if not hasattr(handle, n)]
+    assert not missing, missing
+    assert set(declared_functions()) <= set(lib.EXPORTS)
+
+
+def test_python_binding_has_the_same_names(lib):
+    for n in declared_functions():
+        assert callable(getattr(lib, n)), n
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.status_string(code).startswith("FA_")
+    assert "unknown" in lib.status_string(99)
+    assert lib.fa_abi_version() == 1
+
+
+def test_validation_without_gpu(lib):
+    """Every check below fails before any CUDA call, so it runs on a CPU machine."""
+    A = 1 << 20  # a fake, 16-byte aligned address
+    S = 0
+    assert lib.fa_fwd(0, A, A, A, None, 1, 1, 1, 1, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_fwd(A + 8, A, A, A, None, 1, 1, 1, 1, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_fwd(A, A, A, A, A + 4, 1, 1, 1, 1, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_fwd(A, A, A, A, None, 0, 1, 1, 1, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_fwd(A, A, A, A, None, 1, 1, 1, 0, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_fwd(A, A, A, A, None, 1, 6, 4, 8, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_fwd(A, A, A, A, None, 1, 1, 1, 8, 128, 0.0, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_fwd(A, A, A, A, None, 1, 1, 1, 8, 128, float("nan"), 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_fwd(A, A, A, A, None, 1, 1, 1, 8, 96, 0.1, 0, S) == lib.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd(A, A, A, A, None, 1, 1, 1, 8, 80, 0.1, 0, S) == lib.FA_ERR_UNSUPPORTED
+    assert lib.fa_varlen_fwd(A, A, A, A, None, 0, A, 1, 8, 8, 8, 8, 1, 1, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_varlen_fwd(A, A, A, A, None, A + 2, A, 1, 8, 8, 8, 8, 1, 1, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_varlen_fwd(A, A, A, A, None, A, A, 0, 8, 8, 8, 8, 1, 1, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    ws = lib.fa_paged_workspace_size(2, 4, 128, 100)
+    assert ws > 0
+    # page size other than 16, too-small workspace, too few pages per sequence
+    assert lib.fa_paged_fwd(A, A, A, A, A, A, None, 2, 4, 4, 128, 32, 10, 8, 100, 0.1, 1, A, ws, S) == \
+        lib.FA_ERR_UNSUPPORTED
+    assert lib.fa_paged_fwd(A, A, A, A, A, A, None, 2, 4, 4, 128, 16, 10, 8, 100, 0.1, 1, A, ws - 1, S) == \
+        lib.FA_ERR_INVALID
+    assert lib.fa_paged_fwd(A, A, A, A, A, A, None, 2, 4, 4, 128, 16, 10, 6, 100, 0.1, 1, A, ws, S) == \
+        lib.FA_ERR_INVALID
+    assert lib.fa_paged_fwd(A, A, A, 0, A, A, None, 2, 4, 4, 128, 16, 10, 8, 100, 0.1, 1, A, ws, S) == \
+        lib.FA_ERR_INVALID
+    assert lib.fa_selftest_wait_timeout(0, S) == lib.FA_ERR_INVALID
+
+
+def test_workspace_size_monotone(lib):
+    assert lib.fa_paged_workspace_size(0, 4, 128, 10) == 0
+    assert lib.fa_paged_workspace_size(1, 4, 96, 10) == 0
+    a = lib.fa_paged_workspace_size(64, 32, 128, 16384)
+    b = lib.fa_paged_workspace_size(64, 32, 128, 16385)
+    assert 0 < a <= b and a % 256 == 0

@@ -1,0 +1,115 @@
+"""Paged decode (fa_paged_fwd) and the page gather against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_fwd_gb300 import workloads as W
+from gpu_helpers import assert_lse_close, assert_o_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_paged(fa, pb, H, d, scale, causal=True):
+    B = pb.q.shape[0]
+    Hkv = pb.k_cache.shape[2]
+    o = torch.full_like(pb.q, float("nan"))
+    lse = torch.full((B, H), float("nan"), dtype=torch.float32, device=pb.q.device)
+    ws_bytes = fa.fa_paged_workspace_size(B, H, d, pb.max_seqlen)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=pb.q.device)
+    st = fa.fa_paged_fwd(pb.q, pb.k_cache, pb.v_cache, pb.block_table, pb.seqlens, o, lse, B, H, Hkv, d, 16,
+                         pb.num_pages, pb.block_table.shape[1], pb.max_seqlen, scale, causal, ws, ws_bytes)
+    assert st == fa.FA_OK, fa.status_string(st)
+    return o, lse
+
+
+def check_full(fa, lengths, H, d, seed, Hkv=None, slack=3):
+    pb = W.paged_inputs(lengths, H, d, seed, "cuda", Hkv=Hkv, slack_pages=slack)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_paged(fa, pb, H, d, scale)
+    assert fa.fa_device_status() == fa.FA_OK
+    O_ref, L_ref = oracle.attention_paged(f64(pb.q), f64(pb.k_cache), f64(pb.v_cache), pb.block_table.cpu().numpy(),
+                                          lengths, 16, scale, True)
+    assert_o_close(o, O_ref, f"paged {lengths}")
+    assert_lse_close(lse, L_ref, f"paged {lengths}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_short_and_ragged(fa, d):
+    """seqlen below one page, exactly one page, one past, not a multiple of
+    16, and a length spanning several splits."""
+    check_full(fa, [1, 15, 16, 17, 100, 513, 1300, 2049], 4, d, seed=20 + d)
+
+
+def test_empty_sequence(fa):
+    """seqlen 0: O = 0 and LSE = -inf (no key is visible)."""
+    check_full(fa, [0, 5, 0, 40], 2, 128, seed=21)
+
+
+def test_gqa_decode(fa):
+    check_full(fa, [700, 33, 1], 8, 128, seed=22, Hkv=2)
+
+
+def test_c5_sampled_heads(fa):
+    """The full decode batch (B64, H32, d128, lengths U[512, 16384], random
+    page permutation): every sequence, three sampled heads, each checked by
+    the oracle walking the real block_table over that head's slice of the
+    real pool."""
+    lens = W.c5_lengths()
+    H, d = 32, 128
+    pb = W.paged_inputs(lens, H, d, 1239, "cuda", pool_on_device=True)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_paged(fa, pb, H, d, scale)
+    assert fa.fa_device_status() == fa.FA_OK
+    og, lg = f64(o), f64(lse)
+    bt = pb.block_table.cpu().numpy()
+    for h in (0, 13, 31):
+        kp = f64(pb.k_cache[:, :, h:h + 1, :])
+        vp = f64(pb.v_cache[:, :, h:h + 1, :])
+        O_ref, L_ref = oracle.attention_paged(f64(pb.q[:, h:h + 1]), kp, vp, bt, lens, 16, scale, True)
+        assert_o_close(og[:, h:h + 1], O_ref, f"C5 h{h}")
+        assert_lse_close(lg[:, h:h + 1], L_ref, f"C5 h{h}")
+
+
+def test_gather_bit_exact(fa):
+    """The decode kernels' page walk reads exactly the bytes the host walk of
+    block_table selects."""
+    lens = [1, 16, 17, 250, 999, 2048]
+    pb = W.paged_inputs(lens, 4, 128, 23, "cuda", slack_pages=5)
+    for cache in (pb.k_cache, pb.v_cache):
+        out = torch.zeros((len(lens), pb.max_seqlen, 4, 128), dtype=torch.bfloat16, device="cuda")
+        st = fa.fa_paged_gather(cache, pb.block_table, pb.seqlens, out, len(lens), 4, 128, 16, pb.num_pages,
+                                pb.block_table.shape[1], pb.max_seqlen)
+        assert st == fa.FA_OK
+        assert fa.fa_device_status() == fa.FA_OK
+        host = cache.cpu().view(torch.int16).numpy()
+        got = out.cpu().view(torch.int16).numpy()
+        bt = pb.block_table.cpu().numpy()
+        for b, L in enumerate(lens):
+            ref = oracle.gather_paged_kv(host, bt[b], L, 16)
+            assert np.array_equal(got[b, :L], ref), f"seq {b}"
+
+
+def test_bad_block_table_entry(fa):
+    """An entry outside the pool is skipped and reported; the other sequences
+    are unaffected."""
+    lens = [40, 40]
+    pb = W.paged_inputs(lens, 2, 64, 24, "cuda")
+    bt = pb.block_table.clone()
+    bt[1, 1] = pb.num_pages + 100
+    pb2 = W.PagedBatch(pb.q, pb.k_cache, pb.v_cache, bt, pb.seqlens, pb.lengths, pb.max_seqlen, pb.num_pages)
+    o, lse = run_paged(fa, pb2, 2, 64, 0.125)
+    assert fa.fa_device_status() == fa.FA_ERR_DEVICE_INDEX
+    O_ref, L_ref = oracle.attention_paged(f64(pb.q), f64(pb.k_cache), f64(pb.v_cache), pb.block_table.cpu().numpy(),
+                                          lens, 16, 0.125, True)
+    assert_o_close(o[0:1], O_ref[0:1], "good sequence")
+    assert np.all(np.isfinite(f64(o[1])))
+
+
+def test_deterministic(fa):
+    pb = W.paged_inputs([3000, 17], 4, 128, 25, "cuda")
+    o1, l1 = run_paged(fa, pb, 4, 128, 0.088)
+    o2, l2 = run_paged(fa, pb, 4, 128, 0.088)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
