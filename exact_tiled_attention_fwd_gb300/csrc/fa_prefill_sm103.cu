@@ -1,30 +1,48 @@
 // Prefill forward (dense and varlen) for sm_103a: TMA-staged tiles, tcgen05
 // MMA into tensor memory, one thread per query row for the online softmax.
 //
-// What one CTA computes: one tile of kBlockM = 128 query rows of one
-// (sequence, head), streaming the sequence's K/V in kBlockN = 128-key blocks
-// (tiling, dlog.com.cn "从标准 Attention 到 FlashAttention 与分页执行" §2.1;
-// the (Q block, batch*head) grid of the lqnn.cn page §4.4).  Per K/V block j:
+// What one CTA computes: two tiles of kBlockM = 128 query rows (256 rows) of
+// one (sequence, head), streaming the sequence's K/V in kBlockN = 128-key
+// blocks (tiling, dlog.com.cn "从标准 Attention 到 FlashAttention 与分页执行"
+// §2.1; the (Q block, batch*head) grid of the lqnn.cn page §4.4).  For every
+// K/V block j and each tile t:
 //
-//   S_j  = Q K_j^T                       tcgen05.mma, SMEM x SMEM -> TMEM (fp32)
-//   m'   = max(m, rowmax(S_j * scale))    softmax warps, one thread per row
-//   P_j  = exp(S_j * scale - m)           -> bf16, written back into TMEM
-//   l    = l * exp(m_old - m) + rowsum P_j
-//   O   += P_j V_j                        tcgen05.mma, TMEM x SMEM -> TMEM
+//   S^t_j = Q^t K_j^T                    tcgen05.mma, SMEM x SMEM -> TMEM (fp32)
+//   m'    = max(m, rowmax(S^t_j scale))   softmax warps, one thread per row
+//   P^t_j = exp(S^t_j scale - m)          -> bf16, written back into TMEM
+//   l     = l exp(m_old - m) + rowsum P^t_j
+//   O^t  += P^t_j V_j                     tcgen05.mma, TMEM x SMEM -> TMEM
 //
 // and at the end O / l and lse = m + ln l (online softmax, same page §2.2).
+// The two tiles share every K/V load; while one tile's softmax warps work,
+// the tensor core runs the other tile's products.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K_j / V_j into a 2-slot ring
-//   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
-//   warps 2..5  softmax + correction + epilogue; warp w owns TMEM lanes
-//               32*(w%4) .. +31, i.e. query rows of the tile, one per thread
+// Warp roles (384 threads):
+//   warp 0       TMA producer: both Q tiles once, then K_j / V_j (2-slot rings)
+//   warp 1       allocates tensor memory; lane 0 issues tile 0's tcgen05.mma
+//   warp 2       lane 0 issues tile 1's tcgen05.mma
+//   warp 3       idle
+//   warps 4-7    softmax, correction and epilogue of tile 0
+//   warps 8-11   the same for tile 1
+// Warp w may only touch TMEM lanes 32*(w%4)..+31; within a softmax warp
+// group, thread r of the group owns row r of its tile = TMEM lane r.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
-//   [0,128)    S/P buffer 0     [128,256)  S/P buffer 1     [256,256+d) O
-// P_j (bf16 pairs) overwrites the first 64 columns of its S buffer after the
-// owning thread has read the whole S row.  S is double-buffered so the
-// tensor core computes S_{j+1} while the softmax warps work on S_j.
+//   [0,128) S^0   [128,256) S^1   [256,256+d) O^0   [384,384+d) O^1
+// P^t (bf16 pairs) overwrites the first 64 columns of S^t once the owning
+// thread has read its whole S row.
+//
+// Each tile has its own issuing thread, so one thread's barrier waits (about
+// a hundred cycles each even when the phase is already complete) overlap the
+// other thread's MMA stream and the tensor core's short queue stays fed.  The
+// tiles write disjoint TMEM columns and only read the shared K/V slots, so
+// the two streams need no ordering between them.  Within a tile the order is
+// ... PV^t_j, S^t_{j+1}, ...; tensor-core work of one thread completes in
+// issue order, so when S^t_{j+1} is reported done, PV^t_j (which read P^t_j
+// from the same columns) is done too, and so is every earlier update of
+// O^t: the softmax may rescale O^t in place right after it sees S^t_{j+1}.
+// A K/V slot is released per tile (one empty barrier per tile and slot); the
+// producer waits for each tile that read the slot's previous block.
 //
 // Rescaling: the exponent reference m is only moved when a row's max grows
 // by more than kRescaleThreshold (log2 units); otherwise the old reference is
@@ -48,7 +66,8 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kTiles = 2;  // Q tiles per CTA
 constexpr int kStages = 2;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -58,13 +77,11 @@ constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 64 bf16
 template <int D>
 struct PrefillSmem {
     static constexpr uint32_t kTile = kBlockM * D * 2;  // one Q, K or V tile
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kTile;
-    static constexpr uint32_t kV = kTile * (1 + kStages);
-    static constexpr uint32_t kBar = kTile * (1 + 2 * kStages);
-    // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2],
-    //           s_full[2], p_full[2], o_ready, o_final, mma_done
-    static constexpr uint32_t kNumBars = 16;
+    static constexpr uint32_t kQ = 0;                    // + t * kTile
+    static constexpr uint32_t kK = kTile * kTiles;       // + s * kTile
+    static constexpr uint32_t kV = kK + kTile * kStages;
+    static constexpr uint32_t kBar = kV + kTile * kStages;
+    static constexpr uint32_t kNumBars = 24;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kUsed = kAbort + 4;
@@ -74,19 +91,36 @@ struct PrefillSmem {
 };
 
 enum BarId : uint32_t {
-    B_Q_FULL = 0,
-    B_K_FULL = 1,   // +stage
-    B_K_EMPTY = 3,  // +stage
-    B_V_FULL = 5,   // +stage
-    B_V_EMPTY = 7,  // +stage
-    B_S_FULL = 9,   // +buffer
-    B_P_FULL = 11,  // +buffer
-    B_O_READY = 13,
-    B_O_FINAL = 14,
-    B_MMA_DONE = 15,
+    B_Q_FULL = 0,     // + tile
+    B_K_FULL = 2,     // + stage
+    B_V_FULL = 4,     // + stage
+    B_K_EMPTY = 6,    // + 2 * tile + stage
+    B_V_EMPTY = 10,   // + 2 * tile + stage
+    B_S_FULL = 14,    // + tile
+    B_P_FULL = 16,    // + 2 * tile + half (keys 0-63, 64-127)
+    B_O_FINAL = 20,   // + tile
+    B_MMA_DONE = 22,  // + tile
+    B_COUNT = 24,
 };
 
-__device__ __forceinline__ float fmax3(float a, float b, float c) { return fmaxf(fmaxf(a, b), c); }
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Keys visible to some row of the tile [r0, r_last]: the number of K/V
+// blocks the tile needs (0 if the tile has no valid row or sees no key).
+template <bool CAUSAL>
+__device__ __forceinline__ int tile_blocks(int r0, int r_last, int Lk, int diag) {
+    if (r_last < r0) return 0;
+    int n = (Lk + kBlockN - 1) / kBlockN;
+    if (CAUSAL) {
+        const int max_key = r_last + diag;
+        n = max_key < 0 ? 0 : min(n, max_key / kBlockN + 1);
+    }
+    return n;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -94,7 +128,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     using L = PrefillSmem<D>;
     constexpr int kPanels = D / 64;
-    constexpr uint32_t kOCol = 256;
     constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
     constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
 
@@ -109,7 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seq = blockIdx.z;
     const int h = blockIdx.y;
     const int hk = h / p.group;
-    const int qb = CAUSAL ? (p.num_q_blocks - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    const int nblk = (p.num_q_blocks + 1) / 2;  // 256-row blocks
+    const int qb = CAUSAL ? (nblk - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
 
     // ---- sequence geometry (uniform over the CTA)
     int q_start, Lq, k_start, Lk;
@@ -130,51 +164,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         k_start = seq * p.N;
         Lk = p.N;
     }
-    const int row0 = qb * kBlockM;
+    const int row0 = qb * kBlockM * kTiles;
     if (row0 >= Lq) return;
-    const int row_last = min(Lq, row0 + kBlockM) - 1;
     const int diag = Lk - Lq;  // causal: key j visible to row i iff j <= i + diag
-    int nkv = (Lk + kBlockN - 1) / kBlockN;
-    if (CAUSAL) {
-        const int max_key = row_last + diag;
-        nkv = max_key < 0 ? 0 : min(nkv, max_key / kBlockN + 1);
-    }
-
-    // Rows that see no key at all: O = 0, LSE = -inf (no tensor-core work).
-    if (nkv == 0) {
-        if (warp >= 2) {
-            const int r = (warp & 3) * 32 + lane;
-            const int row = row0 + r;
-            if (row <= row_last) {
-                uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                                       (static_cast<size_t>(q_start + row) * p.H + h) * D);
+    int r_last[kTiles], nb[kTiles];
 #pragma unroll
-                for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0, 0, 0, 0);
-                if (p.lse != nullptr) {
-                    const long long base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
-                    p.lse[base + h * p.lse_head_stride + row] = -__int_as_float(0x7f800000);
-                }
-            }
-        }
-        return;
+    for (int t = 0; t < kTiles; ++t) {
+        r_last[t] = min(Lq, row0 + (t + 1) * kBlockM) - 1;
+        nb[t] = tile_blocks<CAUSAL>(row0 + t * kBlockM, r_last[t], Lk, diag);
     }
+    const int nmax = max(nb[0], nb[1]);
+    const long long lse_base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+
+    // Rows of a tile that sees no key at all: O = 0, LSE = -inf.
+    if (warp >= 4) {
+        const int t = (warp - 4) >> 2;
+        const int row = row0 + t * kBlockM + (warp & 3) * 32 + lane;
+        if (nb[t] == 0 && row <= r_last[t]) {
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + (static_cast<size_t>(q_start + row) * p.H + h) * D);
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0, 0, 0, 0);
+            if (p.lse != nullptr) p.lse[lse_base + h * p.lse_head_stride + row] = NEG_INF;
+        }
+    }
+    if (nmax == 0) return;
 
     // ---- setup: barriers (thread 0), tensor memory (warp 1)
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q_FULL), 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(B_K_FULL + s), 1);
-            mbar_init(bar(B_K_EMPTY + s), 1);
-            mbar_init(bar(B_V_FULL + s), 1);
-            mbar_init(bar(B_V_EMPTY + s), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_S_FULL + b), 1);
-            mbar_init(bar(B_P_FULL + b), 128);
-        }
-        mbar_init(bar(B_O_READY), 1);
-        mbar_init(bar(B_O_FINAL), 1);
-        mbar_init(bar(B_MMA_DONE), 1);
+        for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < 2 * kTiles; ++i) mbar_init(bar(B_P_FULL + i), 4);  // one arrive per softmax warp
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -188,31 +207,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
     const uint64_t lim = p.wait_limit_ns;
 
-    if (warp == 0) {
+    // Register split: 384 threads launch with 168 each (64,512 in all); the
+    // producer/MMA warp group drops and the two softmax groups rise, keeping
+    // the sum: 128*72 + 2*128*216 = 128*56 + 2*128*224 = 64,512.  (The pair
+    // per head dim is the one ptxas allocates without spilling.)
+    constexpr uint32_t kRegsLow = D == 128 ? 72 : 56;
+    constexpr uint32_t kRegsHigh = D == 128 ? 216 : 224;
+    static_assert(128 * kRegsLow + 256 * kRegsHigh <= 168 * kThreads, "register split exceeds the launch");
+    if (warp < 4) {
+        regs_dec<kRegsLow>();
+        if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(bar(B_Q_FULL), L::kTile);
 #pragma unroll
-            for (int pn = 0; pn < kPanels; ++pn)
-                tma_load_3d(sbase + L::kQ + pn * kPanelBytes, &tm_q, bar(B_Q_FULL), pn * 64, h, q_start + row0);
+            for (int t = 0; t < kTiles; ++t) {
+                if (nb[t] == 0) continue;
+                mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kTile);
+#pragma unroll
+                for (int pn = 0; pn < kPanels; ++pn)
+                    tma_load_3d(sbase + L::kQ + t * L::kTile + pn * kPanelBytes, &tm_q, bar(B_Q_FULL + t), pn * 64, h,
+                                q_start + row0 + t * kBlockM);
+            }
             int k_last[kStages], v_last[kStages];
 #pragma unroll
             for (int s = 0; s < kStages; ++s) k_last[s] = v_last[s] = -1;
-            for (int j = 0; j < nkv; ++j) {
+            for (int j = 0; j < nmax; ++j) {
                 const int s = j % kStages;
                 const int n = j / kStages;
                 const int krow = k_start + j * kBlockN;
-                if (n > 0 && !mbar_wait(bar(B_K_EMPTY + s), (n - 1) & 1, abort_flag, p.err, lim)) break;
+                bool ok = true;
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t)  // tiles that read this slot's previous block
+                    if (ok && n > 0 && j - kStages < nb[t])
+                        ok = mbar_wait(bar(B_K_EMPTY + 2 * t + s), (n - 1) & 1, abort_flag, p.err, lim);
+                if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_K_FULL + s), L::kTile);
 #pragma unroll
                 for (int pn = 0; pn < kPanels; ++pn)
                     tma_load_3d(sbase + L::kK + s * L::kTile + pn * kPanelBytes, &tm_k, bar(B_K_FULL + s), pn * 64,
                                 hk, krow);
                 k_last[s] = n;
-                if (n > 0 && !mbar_wait(bar(B_V_EMPTY + s), (n - 1) & 1, abort_flag, p.err, lim)) break;
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t)
+                    if (ok && n > 0 && j - kStages < nb[t])
+                        ok = mbar_wait(bar(B_V_EMPTY + 2 * t + s), (n - 1) & 1, abort_flag, p.err, lim);
+                if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_V_FULL + s), L::kTile);
 #pragma unroll
                 for (int pn = 0; pn < kPanels; ++pn)
@@ -226,119 +268,134 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k_last[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), k_last[s] & 1, lim);
                 if (v_last[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), v_last[s] & 1, lim);
             }
-            mbar_wait_drain(bar(B_Q_FULL), 0, lim);
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t)
+                if (nb[t] > 0) mbar_wait_drain(bar(B_Q_FULL + t), 0, lim);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
-            auto q_desc = [&](int kk) {
-                return sdesc_sw128(sbase + L::kQ + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            };
-            auto k_desc = [&](int s, int kk) {
-                return sdesc_sw128(sbase + L::kK + s * L::kTile + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            };
-            auto v_desc = [&](int s, int kk) {
-                return sdesc_sw128(sbase + L::kV + s * L::kTile + kk * (16 * 128), kPanelBytes, 1024);
-            };
-            auto issue_pv = [&](int i) -> bool {
-                const int s = i % kStages;
-                const int b = i & 1;
-                if (!mbar_wait(bar(B_P_FULL + b), (i >> 1) & 1, abort_flag, p.err, lim)) return false;
-                if (!mbar_wait(bar(B_V_FULL + s), (i / kStages) & 1, abort_flag, p.err, lim)) return false;
-                tc_fence_after();
+    } else if (warp == 1 || warp == 2) {
+        // ================= MMA issuers (warp 1: tile 0, warp 2: tile 1) =================
+        const int t = warp - 1;
+        const int n_t = nb[t];
+        if (lane == 0 && n_t > 0) {
+            // Descriptor bases; a k-step only moves the start address, which
+            // is the low field of the descriptor (addresses stay < 256 KiB, so
+            // the addition never carries out of it).
+            const uint64_t dq = sdesc_sw128(sbase + L::kQ + t * L::kTile, 16, 1024);
+            const uint64_t dk = sdesc_sw128(sbase + L::kK, 16, 1024);
+            const uint64_t dv = sdesc_sw128(sbase + L::kV, kPanelBytes, 1024);
+            const uint32_t t_s = tmem + t * 128;
+            const uint32_t t_o = tmem + 256 + t * 128;
+            bool ok = mbar_wait(bar(B_Q_FULL + t), 0, abort_flag, p.err, lim);
+            // S^t_j = Q^t K_j^T into the S^t columns.
+            auto issue_s = [&](int j) {
+                const int s = j & 1;
+                ok = ok && mbar_wait(bar(B_K_FULL + s), (j >> 1) & 1, abort_flag, p.err, lim);
+                if (!ok) return;
+                const uint64_t b0 = dk + ((s * L::kTile) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts(tmem + kOCol, tmem + b * 128 + kk * 8, v_desc(s, kk), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar(B_V_EMPTY + s));
-                tc_commit(bar(B_O_READY));
-                return true;
-            };
-            bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, p.err, lim);
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int s = j % kStages;
-                const int b = j & 1;
-                if (!mbar_wait(bar(B_K_FULL + s), (j / kStages) & 1, abort_flag, p.err, lim)) {
-                    ok = false;
-                    break;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+                    mma_ss(t_s, dq + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
                 }
-                tc_fence_after();
+                tc_commit(bar(B_S_FULL + t));
+                tc_commit(bar(B_K_EMPTY + 2 * t + s));
+            };
+            // O^t += P^t_j V_j with P^t_j read from the S^t columns.
+            auto issue_pv = [&](int j) {
+                const int s = j & 1;
+                ok = ok && mbar_wait(bar(B_V_FULL + s), (j >> 1) & 1, abort_flag, p.err, lim);
+                const uint64_t b0 = dv + ((s * L::kTile) >> 4);
+                // keys 0-63 as soon as their P is written, then keys 64-127
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + b * 128, q_desc(kk), k_desc(s, kk), kIdescS, kk > 0 ? 1u : 0u);
-                tc_commit(bar(B_K_EMPTY + s));
-                tc_commit(bar(B_S_FULL + b));
-                if (j > 0) ok = issue_pv(j - 1);
+                for (int half = 0; half < 2; ++half) {
+                    ok = ok && mbar_wait(bar(B_P_FULL + 2 * t + half), j & 1, abort_flag, p.err, lim);
+                    if (!ok) return;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k4 = 0; k4 < kBlockN / 32; ++k4) {
+                        const int kk = half * (kBlockN / 32) + k4;
+                        mma_ts(t_o, t_s + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                tc_commit(bar(B_V_EMPTY + 2 * t + s));
+                if (j == n_t - 1) tc_commit(bar(B_O_FINAL + t));
+            };
+            issue_s(0);
+            for (int j = 0; ok && j < n_t; ++j) {
+                issue_pv(j);
+                if (j + 1 < n_t) issue_s(j + 1);
             }
-            if (ok) ok = issue_pv(nkv - 1);
-            if (ok) tc_commit(bar(B_O_FINAL));
-            // Every MMA has finished before tensor memory is released.
-            tc_commit(bar(B_MMA_DONE));
-            mbar_wait_drain(bar(B_MMA_DONE), 0, lim);
+            // Every MMA of this thread has finished before tensor memory is
+            // released.
+            tc_commit(bar(B_MMA_DONE + t));
+            mbar_wait_drain(bar(B_MMA_DONE + t), 0, lim);
         }
         __syncwarp();
+        }
+        // The producer/MMA warp group ends here: join the CTA, then the
+        // allocating warp frees tensor memory.
+        tc_fence_before();
+        cta_sync(kThreads);
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, kTmemCols);
+        }
+        return;
     } else {
+        regs_inc<kRegsHigh>();
         // ================= softmax / correction / epilogue =================
+        const int t = (warp - 4) >> 2;
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // row of the tile == TMEM lane
-        const int row = row0 + r;           // row within the sequence
+        const int r = quarter * 32 + lane;       // row of the tile == TMEM lane
+        const int r0 = row0 + t * kBlockM;
+        const int row = r0 + r;                   // row within the sequence
+        const int n_t = nb[t];
         const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t s_col = t * 128;
+        const uint32_t o_col = 256 + t * 128;
         const float c = p.scale_log2;
-        const float NEG_INF = -__int_as_float(0x7f800000);
         float m_ref = NEG_INF;  // exponent reference (log2 units)
         float l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            const int b = j & 1;
-            if (!warp_wait(bar(B_S_FULL + b), (j >> 1) & 1, abort_flag, p.err, lim)) {
+        bool ok = n_t > 0;
+        for (int j = 0; ok && j < n_t; ++j) {
+            if (!warp_wait(bar(B_S_FULL + t), j & 1, abort_flag, p.err, lim)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float x[kBlockN];
-#pragma unroll
-            for (int ch = 0; ch < kBlockN / 32; ++ch) {
-                uint32_t u[32];
-                tmem_ld32(t_row + b * 128 + ch * 32, u);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[ch * 32 + i] = __uint_as_float(u[i]);
-            }
+            uint32_t u[kBlockN];
+            tmem_ld128(t_row + s_col, u);
             const int kbase = j * kBlockN;
-            const bool need_mask =
-                (kbase + kBlockN > Lk) || (CAUSAL && kbase + kBlockN - 1 > row0 + diag);
+            const bool need_mask = (kbase + kBlockN > Lk) || (CAUSAL && kbase + kBlockN - 1 > r0 + diag);
             if (need_mask) {
                 int lim_c = Lk - 1 - kbase;
                 if (CAUSAL) lim_c = min(lim_c, row + diag - kbase);
 #pragma unroll
                 for (int i = 0; i < kBlockN; ++i)
-                    if (i > lim_c) x[i] = NEG_INF;
+                    if (i > lim_c) u[i] = __float_as_uint(NEG_INF);
             }
             float mx0 = NEG_INF, mx1 = NEG_INF, mx2 = NEG_INF, mx3 = NEG_INF;
 #pragma unroll
             for (int i = 0; i < kBlockN; i += 8) {
-                mx0 = fmax3(mx0, x[i], x[i + 1]);
-                mx1 = fmax3(mx1, x[i + 2], x[i + 3]);
-                mx2 = fmax3(mx2, x[i + 4], x[i + 5]);
-                mx3 = fmax3(mx3, x[i + 6], x[i + 7]);
+                mx0 = fmax3(mx0, __uint_as_float(u[i]), __uint_as_float(u[i + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(u[i + 2]), __uint_as_float(u[i + 3]));
+                mx2 = fmax3(mx2, __uint_as_float(u[i + 4]), __uint_as_float(u[i + 5]));
+                mx3 = fmax3(mx3, __uint_as_float(u[i + 6]), __uint_as_float(u[i + 7]));
             }
-            const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+            const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * c;
             const float m_new = fmaxf(m_ref, m_blk);
             const bool resc = (m_ref != NEG_INF) && (m_new - m_ref > kRescaleThreshold);
             if (__any_sync(0xffffffffu, resc)) {
-                // O must hold P_{j-1} V_{j-1} before it is rescaled.
-                if (!warp_wait(bar(B_O_READY), (j - 1) & 1, abort_flag, p.err, lim)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                // PV^t_{j-1} completed before S^t_j (issue order), so O^t is final.
                 const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t u[32];
-                    tmem_ld32(t_row + kOCol + ch * 32, u);
+                    uint32_t o[32];
+                    tmem_ld32(t_row + o_col + ch * 32, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-                    tmem_st32(t_row + kOCol + ch * 32, u);
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(t_row + o_col + ch * 32, o);
                 }
                 tmem_st_wait();
             }
@@ -348,40 +405,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (m_ref == NEG_INF) m_ref = m_new;
             const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
-            float s0 = 0.f, s1 = 0.f;
+            // P = 2^(S c - mu) in two halves of 64 keys; each half is published
+            // on its own barrier so the P.V product of the first half starts
+            // while the second half is still being exponentiated.
+            const float2 c2 = make_float2(c, c);
+            const float2 nmu2 = make_float2(-mu, -mu);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                uint32_t pk[32];
+            for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2(fmaf(x[ch * 64 + 2 * i], c, -mu));
-                    const float p1 = ex2(fmaf(x[ch * 64 + 2 * i + 1], c, -mu));
-                    s0 += p0;
-                    s1 += p1;
-                    pk[i] = pack_bf16x2(p0, p1);
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int c0 = half * 64 + ch * 32;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[c0 + 2 * i]), __uint_as_float(u[c0 + 2 * i + 1])),
+                                                    c2, nmu2);
+                        const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                        if (i & 1)
+                            acc1 = __fadd2_rn(acc1, e);
+                        else
+                            acc0 = __fadd2_rn(acc0, e);
+                        pk[i] = pack_bf16x2(e.x, e.y);
+                    }
+                    tmem_st16(t_row + s_col + half * 32 + ch * 16, pk);
                 }
-                tmem_st32(t_row + b * 128 + ch * 32, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_P_FULL + 2 * t + half));
             }
-            l += s0 + s1;
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(B_P_FULL + b));
+            l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
         // ---- epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
-        if (ok) ok = warp_wait(bar(B_O_FINAL), 0, abort_flag, p.err, lim);
+        if (ok) ok = warp_wait(bar(B_O_FINAL + t), 0, abort_flag, p.err, lim);
         if (ok) {
             tc_fence_after();
-            const bool store = row <= row_last;
+            const bool store = row <= r_last[t];
             const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
             uint16_t* orow = static_cast<uint16_t*>(p.o) + (static_cast<size_t>(q_start + row) * p.H + h) * D;
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t u[32];
-                tmem_ld32(t_row + kOCol + ch * 32, u);
+                uint32_t o[32];
+                tmem_ld32(t_row + o_col + ch * 32, o);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
                 if (store) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
@@ -391,18 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (store && p.lse != nullptr) {
                 float lg;
                 asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l));
-                const long long base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
-                p.lse[base + h * p.lse_head_stride + row] = l > 0.f ? (m_ref + lg) * kLn2 : NEG_INF;
+                p.lse[lse_base + h * p.lse_head_stride + row] = l > 0.f ? (m_ref + lg) * kLn2 : NEG_INF;
             }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
+    cta_sync(kThreads);
 }
 
 template <int D, bool CAUSAL>
@@ -413,7 +478,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     auto kern = prefill_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_q_blocks, p.H, p.num_seqs);
+    dim3 grid((p.num_q_blocks + 1) / 2, p.H, p.num_seqs);
     kern<<<grid, kThreads, L::kDyn, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
