@@ -25,10 +25,11 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_DEVICE_INDEX = 5
+FA_ERR_SCRATCH_CAPACITY = 6
 
 EXPORTS = (
     "fa_abi_version", "fa_status_string", "fa_fwd", "fa_varlen_fwd", "fa_paged_workspace_size",
-    "fa_paged_fwd", "fa_paged_gather", "fa_device_status", "fa_selftest_wait_timeout",
+    "fa_paged_fwd", "fa_paged_fwd_noalloc", "fa_paged_gather", "fa_device_status", "fa_selftest_wait_timeout",
 )
 
 _lib = None
@@ -62,6 +63,8 @@ def load(path: str | None = None):
     lib.fa_paged_workspace_size.argtypes = [i, i, i, i]
     lib.fa_paged_fwd.restype = i
     lib.fa_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_paged_fwd_noalloc.restype = i
+    lib.fa_paged_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
     lib.fa_paged_gather.restype = i
     lib.fa_paged_gather.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.fa_device_status.restype = i
@@ -123,6 +126,13 @@ def fa_paged_fwd(q, k_cache, v_cache, block_table, seqlens, o, lse, B, H, Hkv, d
     return load().fa_paged_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seqlens), _ptr(o),
                                _ptr(lse), B, H, Hkv, d, page_size, num_pages, max_pages_per_seq, max_seqlen,
                                scale, int(bool(causal)), _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def fa_paged_fwd_noalloc(q, k_cache, v_cache, block_table, seqlens, o, lse, B, H, Hkv, d, page_size, num_pages,
+                         max_pages_per_seq, max_seqlen, scale, causal, stream=None) -> int:
+    return load().fa_paged_fwd_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seqlens),
+                                       _ptr(o), _ptr(lse), B, H, Hkv, d, page_size, num_pages, max_pages_per_seq,
+                                       max_seqlen, scale, int(bool(causal)), _stream(stream))
 
 
 def fa_paged_gather(cache, block_table, seqlens, out, B, Hkv, d, page_size, num_pages, max_pages_per_seq,

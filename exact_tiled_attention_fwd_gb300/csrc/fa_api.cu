@@ -102,6 +102,8 @@ const char* fa_status_string(int status) {
         case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait ran out";
         case FA_ERR_DEVICE_INDEX: return "FA_ERR_DEVICE_INDEX: bad cu_seqlens/seqlens/block_table entry";
+        case FA_ERR_SCRATCH_CAPACITY:
+            return "FA_ERR_SCRATCH_CAPACITY: B*H*(d+2)*4 bytes exceed the fixed 16 MiB decode scratch";
         default: return "unknown fa_status";
     }
 }
@@ -239,6 +241,71 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
     const size_t slots = static_cast<size_t>(B) * H * p.max_splits;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((slots * d * sizeof(float) + 255) & ~size_t(255)));
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(fa::launch_decode(p, d, s), s);
+}
+
+int fa_paged_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                         const int* seqlens, void* o, float* lse, int B, int H, int Hkv, int d, int page_size,
+                         int num_pages, int max_pages_per_seq, int max_seqlen, float scale, int causal,
+                         void* stream) {
+    (void)causal;
+    if (!q || !k_cache || !v_cache || !block_table || !seqlens || !o) return FA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+        return FA_ERR_INVALID;
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || num_pages < 1 || max_pages_per_seq < 1 || max_seqlen < 0 ||
+        !scale_ok(scale))
+        return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (page_size != fa::kPageSize) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_pages_per_seq) * page_size < max_seqlen) return FA_ERR_INVALID;
+    if (B > 65535) return FA_ERR_UNSUPPORTED;
+    // Split the keys so that the per-split partials fit the fixed scratch:
+    // each (sequence, head, split) slot takes d floats of O and two of (m, l).
+    const size_t cap = fa::kStaticScratchBytes;
+    const size_t per_split = static_cast<size_t>(B) * H * (static_cast<size_t>(d) + 2) * sizeof(float);
+    if (per_split + 256 > cap) return FA_ERR_SCRATCH_CAPACITY;
+    const int fit = static_cast<int>((cap - 256) / per_split);
+    int splits = fa::decode_max_splits(max_seqlen);
+    int split_tokens = fa::decode_split_tokens(max_seqlen);
+    if (splits > fit) {
+        split_tokens = (max_seqlen + fit - 1) / fit;
+        split_tokens = (split_tokens + fa::kPageSize - 1) / fa::kPageSize * fa::kPageSize;
+        splits = (max_seqlen + split_tokens - 1) / split_tokens;
+        if (splits < 1) splits = 1;
+    }
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    void* scratch = nullptr;
+    size_t scratch_bytes = 0;
+    if (fa::static_scratch(&scratch, &scratch_bytes) != cudaSuccess) return FA_ERR_CUDA;
+    const size_t slots = static_cast<size_t>(B) * H * splits;
+    const size_t o_bytes = (slots * d * sizeof(float) + 255) & ~size_t(255);
+    if (o_bytes + slots * 2 * sizeof(float) > scratch_bytes) return FA_ERR_SCRATCH_CAPACITY;
+    fa::DecodeParams p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_table = block_table;
+    p.seqlens = seqlens;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages_per_seq;
+    p.max_seqlen = max_seqlen;
+    p.split_tokens = split_tokens;
+    p.max_splits = splits;
+    p.ws_o = static_cast<float*>(scratch);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

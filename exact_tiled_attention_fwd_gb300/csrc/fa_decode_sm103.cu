@@ -19,6 +19,7 @@
 // same rescale rule: M = max m_s, w_s = 2^(m_s - M), l = sum w_s l_s,
 // O = sum w_s o_s / l, LSE = (M + log2 l) ln 2.
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -297,6 +298,35 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
 cudaError_t launch_wait_selftest(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream) {
     wait_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
     return cudaGetLastError();
+}
+
+// Fixed device scratch for fa_paged_fwd_noalloc: the split partials live in
+// this file-scope array instead of a caller workspace.  Every device that
+// loads the library holds kStaticScratchBytes of it until the process exits.
+// Host code may not use the array's name as a device address; the address is
+// looked up once per device with cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_paged_static_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+}  // namespace
+
+cudaError_t static_scratch(void** ptr, size_t* bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_paged_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *ptr = g_scratch_ptr[dev];
+    *bytes = kStaticScratchBytes;
+    return cudaSuccess;
 }
 
 }  // namespace fa

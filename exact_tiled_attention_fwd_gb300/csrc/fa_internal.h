@@ -71,6 +71,11 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream);
 
+// Size of the fixed device scratch used by fa_paged_fwd_noalloc, and the
+// per-device lookup of its address (first call on a device does the lookup).
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+cudaError_t static_scratch(void** ptr, size_t* bytes);
+
 // Decode split sizing shared by the workspace query and the launch.
 inline int decode_split_tokens(int /*max_seqlen*/) { return 512; }
 inline int decode_max_splits(int max_seqlen) {

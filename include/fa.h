@@ -60,7 +60,8 @@ typedef enum fa_status {
     FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d not in {64,128}) */
     FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
     FA_ERR_TIMEOUT = 4,      /* a kernel wait ran out (device error word) */
-    FA_ERR_DEVICE_INDEX = 5  /* a kernel saw a bad cu_seqlens/block_table entry */
+    FA_ERR_DEVICE_INDEX = 5, /* a kernel saw a bad cu_seqlens/block_table entry */
+    FA_ERR_SCRATCH_CAPACITY = 6 /* fa_paged_fwd_noalloc: B*H too large for its fixed scratch */
 } fa_status;
 
 /* Version of this ABI (bumped on any signature change). */
@@ -132,6 +133,35 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
                  int B, int H, int Hkv, int d, int page_size, int num_pages,
                  int max_pages_per_seq, int max_seqlen, float scale, int causal,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_paged_fwd without a caller workspace.  The pages describe no such call:
+ * it exists for callers that cannot allocate device memory at the point they
+ * run attention -- for example an engine that reserves all device memory up
+ * front and hands out none afterwards, a plugin that runs inside someone
+ * else's memory pool, or a decode step that must never call cudaMalloc
+ * because an allocation can synchronise the device.
+ *
+ * Same arguments, layouts and results as fa_paged_fwd, minus workspace and
+ * workspace_bytes.  The split-KV partials go to one fixed 16 MiB device array
+ * inside this library, which every GPU that loads the library keeps until
+ * the process exits.  The keys are split into as few pieces as needed for the
+ * partials, B * H * splits * (d + 2) floats, to fit; a batch with
+ * B * H * (d + 2) * 4 > 16 MiB - 256 bytes (for d = 128: B * H > 32,255)
+ * returns FA_ERR_SCRATCH_CAPACITY.  Nothing in the array needs to start at
+ * zero: every partial the combine step reads is written earlier in the same
+ * call.  All calls in the process share the array, so two calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race and
+ * both results are undefined; order them on one stream.  The first call on a
+ * device looks the array's address up with cudaGetSymbolAddress, so make
+ * that first call before capturing any stream into a graph.  The call itself
+ * allocates nothing (no cudaMalloc, no allocating library routine).
+ */
+int fa_paged_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                         const int* block_table, const int* seqlens, void* o, float* lse,
+                         int B, int H, int Hkv, int d, int page_size, int num_pages,
+                         int max_pages_per_seq, int max_seqlen, float scale, int causal,
+                         void* stream);
 
 /*
  * Copy, through the decode kernels' own page walk, the cached rows every
