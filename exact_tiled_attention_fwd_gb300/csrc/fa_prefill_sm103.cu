@@ -19,8 +19,12 @@
 //
 // Warp roles (384 threads):
 //   warp 0       TMA producer: both Q tiles once, then K_j / V_j (2-slot rings)
-//   warp 1       allocates tensor memory; lane 0 issues tile 0's tcgen05.mma
-//   warp 2       lane 0 issues tile 1's tcgen05.mma
+//   warp 1       allocates tensor memory; issues tile 0's tcgen05.mma
+//   warp 2       issues tile 1's tcgen05.mma
+//                (the whole warp runs the issue loop, with its waits and
+//                descriptor arithmetic warp-uniform; one elected lane
+//                executes each tcgen05.mma / commit, which keeps the
+//                per-MMA issue cost low enough to feed the tensor core)
 //   warp 3       idle
 //   warps 4-7    softmax, correction and epilogue of tile 0
 //   warps 8-11   the same for tile 1
@@ -84,7 +88,8 @@ struct PrefillSmem {
     static constexpr uint32_t kNumBars = 24;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
-    static constexpr uint32_t kUsed = kAbort + 4;
+    static constexpr uint32_t kTurn = kAbort + 4;  // int turn, int done[2]
+    static constexpr uint32_t kUsed = kTurn + 12;
     // Requested dynamic size: 1 KiB alignment slack, and at least 116 KiB so
     // that a single CTA occupies an SM (each CTA takes all 512 TMEM columns).
     static constexpr uint32_t kDyn = (kUsed + 1024) > 118784u ? (kUsed + 1024) : 118784u;
@@ -195,6 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
         for (int i = 0; i < 2 * kTiles; ++i) mbar_init(bar(B_P_FULL + i), 4);  // one arrive per softmax warp
         *abort_flag = 0;
+        volatile int* turn = reinterpret_cast<volatile int*>(smem + L::kTurn);
+        turn[0] = 0;
+        turn[1] = nb[0] == 0;
+        turn[2] = nb[1] == 0;
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -277,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= MMA issuers (warp 1: tile 0, warp 2: tile 1) =================
         const int t = warp - 1;
         const int n_t = nb[t];
-        if (lane == 0 && n_t > 0) {
+        if (n_t > 0) {
             // Descriptor bases; a k-step only moves the start address, which
             // is the low field of the descriptor (addresses stay < 256 KiB, so
             // the addition never carries out of it).
@@ -286,13 +295,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dv = sdesc_sw128(sbase + L::kV, kPanelBytes, 1024);
             const uint32_t t_s = tmem + t * 128;
             const uint32_t t_o = tmem + 256 + t * 128;
-            bool ok = mbar_wait(bar(B_Q_FULL + t), 0, abort_flag, p.err, lim);
+            bool ok = warp_wait(bar(B_Q_FULL + t), 0, abort_flag, p.err, lim);
+            // S^t_j = Q^t K_j^T into the S^t columns.
+            // Waits for the operands of an MMA group; done before taking the
+            // turn so they overlap the other issuer's group.
+            auto wait_s = [&](int j) {
+                ok = ok && warp_wait(bar(B_K_FULL + (j & 1)), (j >> 1) & 1, abort_flag, p.err, lim);
+            };
+            auto wait_pv = [&](int j) {
+                ok = ok && warp_wait(bar(B_V_FULL + (j & 1)), (j >> 1) & 1, abort_flag, p.err, lim);
+                ok = ok && warp_wait(bar(B_P_FULL + 2 * t + 0), j & 1, abort_flag, p.err, lim);
+                ok = ok && warp_wait(bar(B_P_FULL + 2 * t + 1), j & 1, abort_flag, p.err, lim);
+            };
             // S^t_j = Q^t K_j^T into the S^t columns.
             auto issue_s = [&](int j) {
                 const int s = j & 1;
-                ok = ok && mbar_wait(bar(B_K_FULL + s), (j >> 1) & 1, abort_flag, p.err, lim);
-                if (!ok) return;
                 const uint64_t b0 = dk + ((s * L::kTile) >> 4);
+                if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
@@ -300,36 +319,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(bar(B_S_FULL + t));
                 tc_commit(bar(B_K_EMPTY + 2 * t + s));
+                }
+                __syncwarp();
             };
             // O^t += P^t_j V_j with P^t_j read from the S^t columns.
             auto issue_pv = [&](int j) {
                 const int s = j & 1;
-                ok = ok && mbar_wait(bar(B_V_FULL + s), (j >> 1) & 1, abort_flag, p.err, lim);
+                tc_fence_after();
                 const uint64_t b0 = dv + ((s * L::kTile) >> 4);
-                // keys 0-63 as soon as their P is written, then keys 64-127
+                if (elect_one()) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    ok = ok && mbar_wait(bar(B_P_FULL + 2 * t + half), j & 1, abort_flag, p.err, lim);
-                    if (!ok) return;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k4 = 0; k4 < kBlockN / 32; ++k4) {
-                        const int kk = half * (kBlockN / 32) + k4;
-                        mma_ts(t_o, t_s + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts(t_o, t_s + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(bar(B_V_EMPTY + 2 * t + s));
                 if (j == n_t - 1) tc_commit(bar(B_O_FINAL + t));
+                }
+                __syncwarp();
             };
-            issue_s(0);
+            // The two issuers take turns group by group (a tile's P.V of block j
+            // with its S of block j+1), so their instructions never interleave
+            // in the tensor core's queue.  Tile 0's S then completes a group
+            // ahead of tile 1's and the two softmax groups run out of phase,
+            // each hidden behind the other tile's MMAs.  Every wait happens
+            // before the turn is taken; a turn only issues MMAs and commits.
+            volatile int* turn = reinterpret_cast<volatile int*>(smem + L::kTurn);
+            auto take_turn = [&]() {
+                if (turn[0] == t || turn[1 + (t ^ 1)]) return;
+                const uint64_t t0 = globaltimer_ns();
+                for (uint32_t it = 0; turn[0] != t && !turn[1 + (t ^ 1)]; ++it) {
+                    if ((it & 63u) == 63u) {
+                        if (*abort_flag) {
+                            ok = false;
+                            return;
+                        }
+                        if (globaltimer_ns() - t0 > lim) {
+                            *abort_flag = 1;
+                            atomicOr(p.err, FA_DEVERR_TIMEOUT);
+                            ok = false;
+                            return;
+                        }
+                    }
+                }
+            };
+            auto pass_turn = [&]() { __syncwarp(); turn[0] = t ^ 1; };
+            wait_s(0);
+            take_turn();
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) issue_s(0);
+            pass_turn();
             for (int j = 0; ok && j < n_t; ++j) {
+                wait_pv(j);
+                if (j + 1 < n_t) wait_s(j + 1);
+                take_turn();
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
                 issue_pv(j);
                 if (j + 1 < n_t) issue_s(j + 1);
+                pass_turn();
             }
+            turn[1 + t] = 1;  // this tile is done: the other issuer never waits again
+            pass_turn();
             // Every MMA of this thread has finished before tensor memory is
             // released.
-            tc_commit(bar(B_MMA_DONE + t));
-            mbar_wait_drain(bar(B_MMA_DONE + t), 0, lim);
+            if (elect_one()) {
+                tc_commit(bar(B_MMA_DONE + t));
+                mbar_wait_drain(bar(B_MMA_DONE + t), 0, lim);
+            }
+            __syncwarp();
         }
         __syncwarp();
         }
