@@ -43,11 +43,13 @@ SEED_C3 = 1236
 SEED_C5 = 1239
 WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), then paged decode B64 H32 d128, "
             "KV lengths uniform in [512,16384], 16-token pages in a seeded random permutation (fa_paged_fwd)")
-# DRAM bytes (read + write) of one non-causal prefill launch at the headline
-# size, from ncu (see profiles/prefill_kernel_B1H32N8192d128.txt); None when
-# the kernel changed after that capture.
-PREFILL_TRAFFIC_BYTES = None
-DECODE_TRAFFIC_BYTES = None
+# DRAM bytes (read + write) per launch from ncu captures of the current
+# kernels (profiles/prefill_kernel_B1H32N8192d128.md: mean of the non-causal
+# and causal launches; profiles/decode_split_kernel_B16H32d128.md: the
+# 16-sequence capture scaled by cached tokens to the 64-sequence launch).
+# Set to None whenever a kernel changes after its capture.
+PREFILL_TRAFFIC_BYTES = 249.3e6
+DECODE_TRAFFIC_BYTES = 9.29e9
 
 
 def prefill_flops(N, d, H, B, causal):
