@@ -4,11 +4,14 @@ One step = the whole hot path on the headline workloads, inputs resident in
 device memory:
   1. dense prefill, B1 H32 N8192 d128, non-causal        (fa_fwd)
   2. the same, causal                                    (fa_fwd)
-  3. paged decode, B64 H32 d128, KV lengths U[512,16384],
+  3. packed varlen prefill, 16 sequences of U[128,4096]
+     tokens, H32 d64, causal                             (fa_varlen_fwd)
+  4. paged decode, B64 H32 d128, KV lengths U[512,16384],
      16-token pages in a random permutation              (fa_paged_fwd)
 `value` is the prefill throughput in TFLOP/s (4 N^2 d per head, halved for
-causal) over legs 1-2; the decode leg is reported in GB/s of algorithmic
-bytes (every cached K/V byte once, plus q, o, lse and the block_table).
+causal) over legs 1-2; leg 3 is reported in TFLOP/s (same convention, per
+sequence) and leg 4 in GB/s of algorithmic bytes (every cached K/V byte
+once, plus q, o, lse and the block_table).
 L2 is flushed (256 MiB write) before every step; the decode pool (~8.9 GB)
 is far larger than L2 anyway.
 
@@ -40,9 +43,11 @@ METRIC = "attn fwd TFLOP/s & % BF16 peak (N=8192,d=128); paged-decode KV GB/s"
 C3 = dict(B=1, H=32, N=8192, d=128)
 C5 = dict(B=64, H=32, d=128)
 SEED_C3 = 1236
+SEED_C4 = 1238
 SEED_C5 = 1239
-WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), then paged decode B64 H32 d128, "
-            "KV lengths uniform in [512,16384], 16-token pages in a seeded random permutation (fa_paged_fwd)")
+WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), packed varlen prefill 16 x U[128,4096] "
+            "tokens H32 d64 causal (fa_varlen_fwd), then paged decode B64 H32 d128, KV lengths uniform in "
+            "[512,16384], 16-token pages in a seeded random permutation (fa_paged_fwd)")
 # DRAM bytes (read + write) per launch from ncu captures of the current
 # kernels (profiles/prefill_kernel_B1H32N8192d128.md: mean of the non-causal
 # and causal launches; profiles/decode_split_kernel_B16H32d128.md: the
@@ -144,14 +149,22 @@ def barrier(world):
 
 
 def max_over_ranks(world, x: float) -> float:
+    """The slowest rank's value (timing is max-reduced over ranks)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, ms_max: float) -> float:
+    """Whole-job throughput of `world` replicas that each did flops_per_rank
+    in at most ms_max milliseconds (weak scaling: the work grows with N)."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
 # --------------------------------------------------------------------- oracle
@@ -241,10 +254,16 @@ def ours(args, world, rank, local):
     B, H, N, d = C3["B"], C3["H"], C3["N"], C3["d"]
     scale = 1.0 / math.sqrt(d)
     do_prefill = args.case in ("all", "prefill")
+    do_varlen = args.case in ("all", "varlen")
     do_decode = args.case in ("all", "decode")
     q, k, v = W.dense_inputs(B, N, H, d, SEED_C3, dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    vl = W.c4_lengths() if do_varlen else [128]
+    vH, vd = 32, 64
+    vq, vk, vv, vcq, vck = W.varlen_inputs(vl, vH, vd, SEED_C4, dev)
+    vo = torch.empty_like(vq)
+    vlse = torch.empty((vH, vq.shape[0]), dtype=torch.float32, device=dev)
     lens = W.c5_lengths()[: args.decode_batch] if do_decode else [16]
     pb = W.paged_inputs(lens, C5["H"], C5["d"], SEED_C5, dev, pool_on_device=True)
     B5, H5, d5 = len(lens), C5["H"], C5["d"]
@@ -262,6 +281,14 @@ def ours(args, world, rank, local):
         if st != F.FA_OK:
             raise F.FAError(st, "fa_fwd")
 
+    def varlen():
+        if not do_varlen:
+            return
+        st = F.fa_varlen_fwd(vq, vk, vv, vo, vlse, vcq, vck, len(vl), max(vl), max(vl), vq.shape[0], vk.shape[0],
+                             vH, vH, vd, 1.0 / math.sqrt(vd), True, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_varlen_fwd")
+
     def decode():
         if not do_decode:
             return
@@ -274,6 +301,7 @@ def ours(args, world, rank, local):
         flush.zero_()
         prefill(False)
         prefill(True)
+        varlen()
         decode()
     torch.cuda.synchronize()
     st = F.fa_device_status(sp)
@@ -281,7 +309,7 @@ def ours(args, world, rank, local):
         raise F.FAError(st, "warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -296,8 +324,10 @@ def ours(args, world, rank, local):
         e[1].record(stream)
         prefill(True)
         e[2].record(stream)
-        decode()
+        varlen()
         e[3].record(stream)
+        decode()
+        e[4].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
@@ -308,11 +338,14 @@ def ours(args, world, rank, local):
 
     t_nc = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     t_c = sum(e[1].elapsed_time(e[2]) for e in ev) / K
-    t_dec = sum(e[2].elapsed_time(e[3]) for e in ev) / K
-    t_nc, t_c, t_dec = (max_over_ranks(world, x) for x in (t_nc, t_c, t_dec))
+    t_var = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    t_dec = sum(e[3].elapsed_time(e[4]) for e in ev) / K
+    t_nc, t_c, t_var, t_dec = (max_over_ranks(world, x) for x in (t_nc, t_c, t_var, t_dec))
+    f_var = sum(4.0 * L * L * vd * vH / 2 for L in vl)
+    var_tflops = f_var / (t_var * 1e-3) / 1e12 if do_varlen else None
     f_nc = prefill_flops(N, d, H, B, False)
     f_c = prefill_flops(N, d, H, B, True)
-    tflops = (f_nc + f_c) / ((t_nc + t_c) * 1e-3) / 1e12
+    tflops = job_tflops(1, f_nc + f_c, t_nc + t_c)  # per replica; the job value multiplies by world
     kv_bytes = float(sum(lens)) * H5 * d5 * 2 * 2
     dec_bytes = kv_bytes + 2 * B5 * H5 * d5 * 2 + B5 * H5 * 4 + sum((L + 15) // 16 for L in lens) * 4
     gbs = dec_bytes / (t_dec * 1e-3) / 1e9
@@ -320,8 +353,8 @@ def ours(args, world, rank, local):
 
     if args.case != "all":
         if rank == 0:
-            print(json.dumps({"case": args.case, "prefill_ms": [t_nc, t_c], "decode_ms": t_dec,
-                              "prefill_tflops": tflops if do_prefill else None,
+            print(json.dumps({"case": args.case, "prefill_ms": [t_nc, t_c], "varlen_ms": t_var, "decode_ms": t_dec,
+                              "prefill_tflops": tflops if do_prefill else None, "varlen_tflops": var_tflops,
                               "decode_gbs": gbs if do_decode else None}), flush=True)
         return
 
@@ -367,12 +400,12 @@ def ours(args, world, rank, local):
         return
     line = {
         "metric": METRIC,
-        "value": tflops * world,
+        "value": job_tflops(world, f_nc + f_c, t_nc + t_c),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": t_nc + t_c + t_dec,
+        "ms_per_step": t_nc + t_c + t_var + t_dec,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -385,6 +418,8 @@ def ours(args, world, rank, local):
         "legs": {
             "prefill_noncausal": {"ms": t_nc, "tflops": f_nc / (t_nc * 1e-3) / 1e12},
             "prefill_causal": {"ms": t_c, "tflops": f_c / (t_c * 1e-3) / 1e12},
+            "varlen_causal_d64": {"ms": t_var, "tflops": var_tflops, "frac_bf16_peak": var_tflops / peak_tf,
+                                  "tokens": int(sum(vl))},
             "paged_decode": {"ms": t_dec, "gbs": gbs, "frac_hbm": gbs / peak_gbs, "kv_tokens": int(sum(lens))},
         },
         "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": tflops, "peak": peak_tf,
@@ -395,7 +430,7 @@ def ours(args, world, rank, local):
                             "traffic": DECODE_TRAFFIC_BYTES, "peak_source": f"{peak_src} HBM copy"},
         "e2e": {"value": e2e_tflops * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "prefill legs with q,k,v copied from pinned host memory and O, LSE copied back each step"},
-        "gpu_launches": 4 * K,
+        "gpu_launches": 5 * K,
         "clocks": clk,
         "wall_s_timed": wall,
     }
@@ -412,7 +447,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--case", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode"], default="all",
                     help="run only one leg (for profiling); prints a short line instead of the bench line")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences of the decode leg (profiling)")
     args = ap.parse_args()
