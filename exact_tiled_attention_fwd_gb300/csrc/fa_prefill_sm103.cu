@@ -144,11 +144,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Dispatch order.  Non-causal: grid (256-row Q block, head, sequence),
+    // blocks fastest, so the CTAs resident at once cover few heads and their
+    // K/V stay in L2.  Causal: grid (head, block, sequence), heads fastest
+    // with blocks from the last (most keys) to the first, so the heavy work
+    // is handed out first across all heads and the light work last.
     const int seq = blockIdx.z;
-    const int h = blockIdx.y;
-    const int hk = h / p.group;
     const int nblk = (p.num_q_blocks + 1) / 2;  // 256-row blocks
-    const int qb = CAUSAL ? (nblk - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    const int h = CAUSAL ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
+    const int hk = h / p.group;
+    const int qb = CAUSAL ? (nblk - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.x);
 
     // ---- sequence geometry (uniform over the CTA)
     int q_start, Lq, k_start, Lk;
@@ -534,7 +539,8 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     auto kern = prefill_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
     if (e != cudaSuccess) return e;
-    dim3 grid((p.num_q_blocks + 1) / 2, p.H, p.num_seqs);
+    const int nblk = (p.num_q_blocks + 1) / 2;
+    const dim3 grid = CAUSAL ? dim3(p.H, nblk, p.num_seqs) : dim3(nblk, p.H, p.num_seqs);
     kern<<<grid, kThreads, L::kDyn, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
