@@ -9,16 +9,15 @@
 //
 //   S^t_j = Q^t K_j^T                    tcgen05.mma, SMEM x SMEM -> TMEM (fp32)
 //   m'    = max(m, rowmax(S^t_j scale))   softmax warps, one thread per row
-//   P^t_j = exp(S^t_j scale - m)          -> bf16, written back into TMEM
+//   P^t_j = exp(S^t_j scale - m)          -> bf16 rows into shared memory
 //   l     = l exp(m_old - m) + rowsum P^t_j
-//   O^t  += P^t_j V_j                     tcgen05.mma, TMEM x SMEM -> TMEM
+//   O^t  += P^t_j V_j                     tcgen05.mma, SMEM x SMEM -> TMEM
 //
 // and at the end O / l and lse = m + ln l (online softmax, same page §2.2).
-// The two tiles share every K/V load; while one tile's softmax warps work,
-// the tensor core runs the other tile's products.
+// The two tiles share every K/V load.
 //
 // Warp roles (384 threads):
-//   warp 0       TMA producer: both Q tiles once, then K_j / V_j (2-slot rings)
+//   warp 0       TMA producer: both Q tiles once, then the K/V ring
 //   warp 1       allocates tensor memory; issues tile 0's tcgen05.mma
 //   warp 2       issues tile 1's tcgen05.mma
 //                (the whole warp runs the issue loop, with its waits and
@@ -33,20 +32,23 @@
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128) S^0   [128,256) S^1   [256,256+d) O^0   [384,384+d) O^1
-// P^t (bf16 pairs) overwrites the first 64 columns of S^t once the owning
-// thread has read its whole S row.
 //
-// Each tile has its own issuing thread, so one thread's barrier waits (about
-// a hundred cycles each even when the phase is already complete) overlap the
-// other thread's MMA stream and the tensor core's short queue stays fed.  The
-// tiles write disjoint TMEM columns and only read the shared K/V slots, so
-// the two streams need no ordering between them.  Within a tile the order is
-// ... PV^t_j, S^t_{j+1}, ...; tensor-core work of one thread completes in
-// issue order, so when S^t_{j+1} is reported done, PV^t_j (which read P^t_j
-// from the same columns) is done too, and so is every earlier update of
-// O^t: the softmax may rescale O^t in place right after it sees S^t_{j+1}.
-// A K/V slot is released per tile (one empty barrier per tile and slot); the
-// producer waits for each tile that read the slot's previous block.
+// Decoupled S and P.  P^t_j goes to its own shared-memory tile (128 rows x
+// 128 keys, the K-major 128-byte-swizzled layout the MMA reads), not back
+// into tensor memory, so S^t's columns are free as soon as the softmax has
+// read them.  The softmax signals that right after its tensor-memory load,
+// and the issuer starts S^t_{j+1} while the softmax is still computing
+// P^t_j.  Per tile the issue order is S_0, S_1, PV_0, S_2, PV_1, ...; the
+// softmax warps of a tile therefore run block after block without waiting
+// on the tensor core, and the tensor core works on both tiles' S and P.V
+// products underneath.
+//
+// Shared memory: Q (two tiles), P (two tiles), and a ring of kSlots K/V
+// tiles loaded in the order K_0, K_1, V_0, K_2, V_1, K_3, ... (K one block
+// ahead of V, the order the MMAs consume them).  A slot is released per tile
+// (one empty barrier per tile and slot, committed after that tile's MMAs
+// that read it); the producer waits for every tile that read the slot's
+// previous occupant.
 //
 // Rescaling: the exponent reference m is only moved when a row's max grows
 // by more than kRescaleThreshold (log2 units); otherwise the old reference is
@@ -72,24 +74,25 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kTiles = 2;  // Q tiles per CTA
-constexpr int kStages = 2;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kMaxSlots = 6;
 
 template <int D>
 struct PrefillSmem {
-    static constexpr uint32_t kTile = kBlockM * D * 2;  // one Q, K or V tile
-    static constexpr uint32_t kQ = 0;                    // + t * kTile
-    static constexpr uint32_t kK = kTile * kTiles;       // + s * kTile
-    static constexpr uint32_t kV = kK + kTile * kStages;
-    static constexpr uint32_t kBar = kV + kTile * kStages;
-    static constexpr uint32_t kNumBars = 24;
+    static constexpr uint32_t kTile = kBlockM * D * 2;         // one Q, K or V tile
+    static constexpr uint32_t kPTile = kBlockM * kBlockN * 2;  // one P tile
+    static constexpr int kSlots = D == 128 ? 3 : 6;            // K/V ring
+    static constexpr uint32_t kQ = 0;                           // + t * kTile
+    static constexpr uint32_t kP = kQ + kTiles * kTile;         // + t * kPTile
+    static constexpr uint32_t kKV = kP + kTiles * kPTile;       // + slot * kTile
+    static constexpr uint32_t kBar = kKV + kSlots * kTile;
+    static constexpr uint32_t kNumBars = 40;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
-    static constexpr uint32_t kTurn = kAbort + 4;  // int turn, int done[2]
-    static constexpr uint32_t kUsed = kTurn + 12;
+    static constexpr uint32_t kUsed = kAbort + 4;
     // Requested dynamic size: 1 KiB alignment slack, and at least 116 KiB so
     // that a single CTA occupies an SM (each CTA takes all 512 TMEM columns).
     static constexpr uint32_t kDyn = (kUsed + 1024) > 118784u ? (kUsed + 1024) : 118784u;
@@ -97,15 +100,15 @@ struct PrefillSmem {
 
 enum BarId : uint32_t {
     B_Q_FULL = 0,     // + tile
-    B_K_FULL = 2,     // + stage
-    B_V_FULL = 4,     // + stage
-    B_K_EMPTY = 6,    // + 2 * tile + stage
-    B_V_EMPTY = 10,   // + 2 * tile + stage
-    B_S_FULL = 14,    // + tile
-    B_P_FULL = 16,    // + 2 * tile + half (keys 0-63, 64-127)
-    B_O_FINAL = 20,   // + tile
-    B_MMA_DONE = 22,  // + tile
-    B_COUNT = 24,
+    B_KV_FULL = 2,    // + slot
+    B_KV_EMPTY = 8,   // + tile * kMaxSlots + slot
+    B_S_FULL = 20,    // + tile: S^t_j is in TMEM
+    B_S_FREE = 22,    // + tile: the softmax has read S^t_j
+    B_P_FULL = 24,    // + tile: P^t_j is in shared memory
+    B_P_EMPTY = 26,   // + tile: PV^t_j is done (P tile free, O^t current)
+    B_O_FINAL = 28,   // + tile
+    B_MMA_DONE = 30,  // + tile
+    B_COUNT = 32,
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -113,6 +116,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Position of K_j / V_j in the load sequence K_0, K_1, V_0, K_2, V_1, ...,
+// K_{n-1}, V_{n-2}, V_{n-1} (n = blocks the CTA streams).
+__device__ __forceinline__ int pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int pos_v(int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; }
 
 // Keys visible to some row of the tile [r0, r_last]: the number of K/V
 // blocks the tile needs (0 if the tile has no valid row or sees no key).
@@ -133,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     using L = PrefillSmem<D>;
     constexpr int kPanels = D / 64;
+    constexpr int kSlots = L::kSlots;
     constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
     constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
 
@@ -203,12 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- setup: barriers (thread 0), tensor memory (warp 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
-        for (int i = 0; i < 2 * kTiles; ++i) mbar_init(bar(B_P_FULL + i), 4);  // one arrive per softmax warp
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(bar(B_S_FREE + t), 4);  // one arrive per softmax warp
+            mbar_init(bar(B_P_FULL + t), 4);
+        }
         *abort_flag = 0;
-        volatile int* turn = reinterpret_cast<volatile int*>(smem + L::kTurn);
-        turn[0] = 0;
-        turn[1] = nb[0] == 0;
-        turn[2] = nb[1] == 0;
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -231,168 +243,142 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         regs_dec<kRegsLow>();
         if (warp == 0) {
-        // ================= TMA producer =================
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
+            // ================= TMA producer =================
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
 #pragma unroll
-            for (int t = 0; t < kTiles; ++t) {
-                if (nb[t] == 0) continue;
-                mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kTile);
+                for (int t = 0; t < kTiles; ++t) {
+                    if (nb[t] == 0) continue;
+                    mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kTile);
 #pragma unroll
-                for (int pn = 0; pn < kPanels; ++pn)
-                    tma_load_3d(sbase + L::kQ + t * L::kTile + pn * kPanelBytes, &tm_q, bar(B_Q_FULL + t), pn * 64, h,
-                                q_start + row0 + t * kBlockM);
-            }
-            int k_last[kStages], v_last[kStages];
+                    for (int pn = 0; pn < kPanels; ++pn)
+                        tma_load_3d(sbase + L::kQ + t * L::kTile + pn * kPanelBytes, &tm_q, bar(B_Q_FULL + t), pn * 64,
+                                    h, q_start + row0 + t * kBlockM);
+                }
+                // Per (tile, slot): whether the tile reads the slot's current
+                // occupant, and the parity of how many occupants it has read.
+                uint32_t used = 0, par = 0;  // bit t * kMaxSlots + slot
+                int last_fill[kMaxSlots];
 #pragma unroll
-            for (int s = 0; s < kStages; ++s) k_last[s] = v_last[s] = -1;
-            for (int j = 0; j < nmax; ++j) {
-                const int s = j % kStages;
-                const int n = j / kStages;
-                const int krow = k_start + j * kBlockN;
+                for (int s = 0; s < kMaxSlots; ++s) last_fill[s] = -1;
                 bool ok = true;
+                auto load = [&](int i, bool is_k, int j) {
+                    const int s = i % kSlots;
 #pragma unroll
-                for (int t = 0; t < kTiles; ++t)  // tiles that read this slot's previous block
-                    if (ok && n > 0 && j - kStages < nb[t])
-                        ok = mbar_wait(bar(B_K_EMPTY + 2 * t + s), (n - 1) & 1, abort_flag, p.err, lim);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar(B_K_FULL + s), L::kTile);
+                    for (int t = 0; t < kTiles; ++t) {
+                        const uint32_t bit = 1u << (t * kMaxSlots + s);
+                        if (ok && (used & bit))  // wait until tile t released the previous occupant
+                            ok = mbar_wait(bar(B_KV_EMPTY + t * kMaxSlots + s), ((par & bit) ? 0u : 1u), abort_flag,
+                                           p.err, lim);
+                    }
+                    if (!ok) return;
+                    mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kTile);
+                    const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
 #pragma unroll
-                for (int pn = 0; pn < kPanels; ++pn)
-                    tma_load_3d(sbase + L::kK + s * L::kTile + pn * kPanelBytes, &tm_k, bar(B_K_FULL + s), pn * 64,
-                                hk, krow);
-                k_last[s] = n;
+                    for (int pn = 0; pn < kPanels; ++pn)
+                        tma_load_3d(sbase + L::kKV + s * L::kTile + pn * kPanelBytes, map, bar(B_KV_FULL + s), pn * 64, hk,
+                                    k_start + j * kBlockN);
+                    last_fill[s] = i / kSlots;
 #pragma unroll
-                for (int t = 0; t < kTiles; ++t)
-                    if (ok && n > 0 && j - kStages < nb[t])
-                        ok = mbar_wait(bar(B_V_EMPTY + 2 * t + s), (n - 1) & 1, abort_flag, p.err, lim);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar(B_V_FULL + s), L::kTile);
-#pragma unroll
-                for (int pn = 0; pn < kPanels; ++pn)
-                    tma_load_3d(sbase + L::kV + s * L::kTile + pn * kPanelBytes, &tm_v, bar(B_V_FULL + s), pn * 64,
-                                hk, krow);
-                v_last[s] = n;
-            }
-            // Drain: every copy this CTA issued lands before the CTA exits.
-#pragma unroll
-            for (int s = 0; s < kStages; ++s) {
-                if (k_last[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), k_last[s] & 1, lim);
-                if (v_last[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), v_last[s] & 1, lim);
-            }
-#pragma unroll
-            for (int t = 0; t < kTiles; ++t)
-                if (nb[t] > 0) mbar_wait_drain(bar(B_Q_FULL + t), 0, lim);
-        }
-        __syncwarp();
-    } else if (warp == 1 || warp == 2) {
-        // ================= MMA issuers (warp 1: tile 0, warp 2: tile 1) =================
-        const int t = warp - 1;
-        const int n_t = nb[t];
-        if (n_t > 0) {
-            // Descriptor bases; a k-step only moves the start address, which
-            // is the low field of the descriptor (addresses stay < 256 KiB, so
-            // the addition never carries out of it).
-            const uint64_t dq = sdesc_sw128(sbase + L::kQ + t * L::kTile, 16, 1024);
-            const uint64_t dk = sdesc_sw128(sbase + L::kK, 16, 1024);
-            const uint64_t dv = sdesc_sw128(sbase + L::kV, kPanelBytes, 1024);
-            const uint32_t t_s = tmem + t * 128;
-            const uint32_t t_o = tmem + 256 + t * 128;
-            bool ok = warp_wait(bar(B_Q_FULL + t), 0, abort_flag, p.err, lim);
-            // S^t_j = Q^t K_j^T into the S^t columns.
-            // Waits for the operands of an MMA group; done before taking the
-            // turn so they overlap the other issuer's group.
-            auto wait_s = [&](int j) {
-                ok = ok && warp_wait(bar(B_K_FULL + (j & 1)), (j >> 1) & 1, abort_flag, p.err, lim);
-            };
-            auto wait_pv = [&](int j) {
-                ok = ok && warp_wait(bar(B_V_FULL + (j & 1)), (j >> 1) & 1, abort_flag, p.err, lim);
-                ok = ok && warp_wait(bar(B_P_FULL + 2 * t + 0), j & 1, abort_flag, p.err, lim);
-                ok = ok && warp_wait(bar(B_P_FULL + 2 * t + 1), j & 1, abort_flag, p.err, lim);
-            };
-            // S^t_j = Q^t K_j^T into the S^t columns.
-            auto issue_s = [&](int j) {
-                const int s = j & 1;
-                const uint64_t b0 = dk + ((s * L::kTile) >> 4);
-                if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
-                    mma_ss(t_s, dq + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bar(B_S_FULL + t));
-                tc_commit(bar(B_K_EMPTY + 2 * t + s));
-                }
-                __syncwarp();
-            };
-            // O^t += P^t_j V_j with P^t_j read from the S^t columns.
-            auto issue_pv = [&](int j) {
-                const int s = j & 1;
-                tc_fence_after();
-                const uint64_t b0 = dv + ((s * L::kTile) >> 4);
-                if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts(t_o, t_s + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar(B_V_EMPTY + 2 * t + s));
-                if (j == n_t - 1) tc_commit(bar(B_O_FINAL + t));
-                }
-                __syncwarp();
-            };
-            // The two issuers take turns group by group (a tile's P.V of block j
-            // with its S of block j+1), so their instructions never interleave
-            // in the tensor core's queue.  Tile 0's S then completes a group
-            // ahead of tile 1's and the two softmax groups run out of phase,
-            // each hidden behind the other tile's MMAs.  Every wait happens
-            // before the turn is taken; a turn only issues MMAs and commits.
-            volatile int* turn = reinterpret_cast<volatile int*>(smem + L::kTurn);
-            auto take_turn = [&]() {
-                if (turn[0] == t || turn[1 + (t ^ 1)]) return;
-                const uint64_t t0 = globaltimer_ns();
-                for (uint32_t it = 0; turn[0] != t && !turn[1 + (t ^ 1)]; ++it) {
-                    if ((it & 63u) == 63u) {
-                        if (*abort_flag) {
-                            ok = false;
-                            return;
-                        }
-                        if (globaltimer_ns() - t0 > lim) {
-                            *abort_flag = 1;
-                            atomicOr(p.err, FA_DEVERR_TIMEOUT);
-                            ok = false;
-                            return;
+                    for (int t = 0; t < kTiles; ++t) {
+                        const uint32_t bit = 1u << (t * kMaxSlots + s);
+                        if (j < nb[t]) {
+                            used |= bit;
+                            par ^= bit;
+                        } else {
+                            used &= ~bit;
                         }
                     }
+                };
+                load(pos_k(0), true, 0);
+                for (int j = 0; ok && j < nmax; ++j) {
+                    if (j + 1 < nmax) load(pos_k(j + 1), true, j + 1);
+                    load(pos_v(j, nmax), false, j);
                 }
-            };
-            auto pass_turn = [&]() { __syncwarp(); turn[0] = t ^ 1; };
-            wait_s(0);
-            take_turn();
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) issue_s(0);
-            pass_turn();
-            for (int j = 0; ok && j < n_t; ++j) {
-                wait_pv(j);
-                if (j + 1 < n_t) wait_s(j + 1);
-                take_turn();
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                issue_pv(j);
-                if (j + 1 < n_t) issue_s(j + 1);
-                pass_turn();
-            }
-            turn[1 + t] = 1;  // this tile is done: the other issuer never waits again
-            pass_turn();
-            // Every MMA of this thread has finished before tensor memory is
-            // released.
-            if (elect_one()) {
-                tc_commit(bar(B_MMA_DONE + t));
-                mbar_wait_drain(bar(B_MMA_DONE + t), 0, lim);
+                // Drain: every copy this CTA issued lands before the CTA exits.
+#pragma unroll
+                for (int s = 0; s < kMaxSlots; ++s)
+                    if (s < kSlots && last_fill[s] >= 0) mbar_wait_drain(bar(B_KV_FULL + s), last_fill[s] & 1, lim);
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t)
+                    if (nb[t] > 0) mbar_wait_drain(bar(B_Q_FULL + t), 0, lim);
             }
             __syncwarp();
-        }
-        __syncwarp();
+        } else if (warp == 1 || warp == 2) {
+            // ================= MMA issuers (warp 1: tile 0, warp 2: tile 1) =================
+            const int t = warp - 1;
+            const int n_t = nb[t];
+            if (n_t > 0) {
+                // Descriptor bases; a k-step only moves the start address, which
+                // is the low field of the descriptor (addresses stay < 256 KiB, so
+                // the addition never carries out of it).
+                const uint64_t dq = sdesc_sw128(sbase + L::kQ + t * L::kTile, 16, 1024);
+                const uint64_t dp = sdesc_sw128(sbase + L::kP + t * L::kPTile, 16, 1024);
+                const uint64_t dk = sdesc_sw128(sbase + L::kKV, 16, 1024);
+                const uint64_t dv = sdesc_sw128(sbase + L::kKV, kPanelBytes, 1024);
+                const uint32_t t_s = tmem + t * 128;
+                const uint32_t t_o = tmem + 256 + t * 128;
+                bool ok = warp_wait(bar(B_Q_FULL + t), 0, abort_flag, p.err, lim);
+                auto wait_item = [&](int i) {
+                    ok = ok && warp_wait(bar(B_KV_FULL + i % kSlots), (i / kSlots) & 1, abort_flag, p.err, lim);
+                };
+                // S^t_j = Q^t K_j^T into the S^t columns.
+                auto issue_s = [&](int j) {
+                    const int s = pos_k(j) % kSlots;
+                    const uint64_t b0 = dk + ((s * L::kTile) >> 4);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+                            mma_ss(t_s, dq + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(B_S_FULL + t));
+                        tc_commit(bar(B_KV_EMPTY + t * kMaxSlots + s));
+                    }
+                    __syncwarp();
+                };
+                // O^t += P^t_j V_j, P from shared memory.
+                auto issue_pv = [&](int j) {
+                    const int s = pos_v(j, nmax) % kSlots;
+                    const uint64_t b0 = dv + ((s * L::kTile) >> 4);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                            const uint32_t offp = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+                            mma_ss(t_o, dp + offp, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(bar(B_P_EMPTY + t));
+                        tc_commit(bar(B_KV_EMPTY + t * kMaxSlots + s));
+                        if (j == n_t - 1) tc_commit(bar(B_O_FINAL + t));
+                    }
+                    __syncwarp();
+                };
+                wait_item(pos_k(0));
+                if (ok) issue_s(0);
+                for (int j = 0; ok && j < n_t; ++j) {
+                    if (j + 1 < n_t) {
+                        // S^t_{j+1} overwrites S^t_j: wait until the softmax has read it.
+                        ok = ok && warp_wait(bar(B_S_FREE + t), j & 1, abort_flag, p.err, lim);
+                        wait_item(pos_k(j + 1));
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(j + 1);
+                    }
+                    ok = ok && warp_wait(bar(B_P_FULL + t), j & 1, abort_flag, p.err, lim);
+                    wait_item(pos_v(j, nmax));
+                    if (!ok) break;
+                    issue_pv(j);
+                }
+                // Every MMA of this warp has finished before tensor memory is
+                // released.
+                if (elect_one()) {
+                    tc_commit(bar(B_MMA_DONE + t));
+                    mbar_wait_drain(bar(B_MMA_DONE + t), 0, lim);
+                }
+                __syncwarp();
+            }
         }
         // The producer/MMA warp group ends here: join the CTA, then the
         // allocating warp frees tensor memory.
@@ -415,6 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t s_col = t * 128;
         const uint32_t o_col = 256 + t * 128;
+        // this row of the P tile (128-byte swizzle: chunk c of a 128-byte
+        // panel row lands at (c ^ (row % 8)) * 16)
+        const uint32_t p_row = sbase + L::kP + t * L::kPTile + r * 128;
+        const uint32_t p_sw = static_cast<uint32_t>(r & 7);
         const float c = p.scale_log2;
         float m_ref = NEG_INF;  // exponent reference (log2 units)
         float l = 0.f;
@@ -427,6 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             uint32_t u[kBlockN];
             tmem_ld128(t_row + s_col, u);
+            // S^t_j is in registers: the issuer may overwrite its columns.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_S_FREE + t));
             const int kbase = j * kBlockN;
             const bool need_mask = (kbase + kBlockN > Lk) || (CAUSAL && kbase + kBlockN - 1 > r0 + diag);
             if (need_mask) {
@@ -447,9 +441,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * c;
             const float m_new = fmaxf(m_ref, m_blk);
             const bool resc = (m_ref != NEG_INF) && (m_new - m_ref > kRescaleThreshold);
+            const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
+            if (resc || m_ref == NEG_INF) m_ref = m_new;
+            const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
+            // P = 2^(S c - mu) as bf16 pairs, kept in registers until the P
+            // tile is free, so the wait for the previous P.V overlaps this.
+            const float2 c2 = make_float2(c, c);
+            const float2 nmu2 = make_float2(-mu, -mu);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            uint32_t pk[kBlockN / 2];
+#pragma unroll
+            for (int i = 0; i < kBlockN / 2; ++i) {
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2, nmu2);
+                const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                if (i & 1)
+                    acc1 = __fadd2_rn(acc1, e);
+                else
+                    acc0 = __fadd2_rn(acc0, e);
+                pk[i] = pack_bf16x2(e.x, e.y);
+            }
+            l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+            // PV^t_{j-1} must be done before the P tile is rewritten or O^t is
+            // rescaled.  (PV^t_{j-2} is known done: it was issued before
+            // S^t_j.)
+            if (j > 0 && !warp_wait(bar(B_P_EMPTY + t), (j - 1) & 1, abort_flag, p.err, lim)) {
+                ok = false;
+                break;
+            }
             if (__any_sync(0xffffffffu, resc)) {
-                // PV^t_{j-1} completed before S^t_j (issue order), so O^t is final.
-                const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
+                tc_fence_after();
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t o[32];
@@ -460,43 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
             }
-            if (resc) {
-                l *= ex2(m_ref - m_new);
-                m_ref = m_new;
+            // keys 8c .. 8c+7 are 16-byte chunk c % 8 of panel c / 8
+#pragma unroll
+            for (int cc = 0; cc < kBlockN / 8; ++cc) {
+                const uint32_t addr = p_row + (cc >> 3) * kPanelBytes + ((static_cast<uint32_t>(cc & 7) ^ p_sw) << 4);
+                st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             }
-            if (m_ref == NEG_INF) m_ref = m_new;
-            const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
-            // P = 2^(S c - mu) in two halves of 64 keys; each half is published
-            // on its own barrier so the P.V product of the first half starts
-            // while the second half is still being exponentiated.
-            const float2 c2 = make_float2(c, c);
-            const float2 nmu2 = make_float2(-mu, -mu);
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    const int c0 = half * 64 + ch * 32;
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[c0 + 2 * i]), __uint_as_float(u[c0 + 2 * i + 1])),
-                                                    c2, nmu2);
-                        const float2 e = make_float2(ex2(x.x), ex2(x.y));
-                        if (i & 1)
-                            acc1 = __fadd2_rn(acc1, e);
-                        else
-                            acc0 = __fadd2_rn(acc0, e);
-                        pk[i] = pack_bf16x2(e.x, e.y);
-                    }
-                    tmem_st16(t_row + s_col + half * 32 + ch * 16, pk);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_P_FULL + 2 * t + half));
-            }
-            l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+            // make the P rows visible to the tensor core, then publish
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + t));
         }
         // ---- epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
         if (ok) ok = warp_wait(bar(B_O_FINAL + t), 0, abort_flag, p.err, lim);
@@ -536,6 +529,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                      cudaStream_t stream) {
     using L = PrefillSmem<D>;
     static_assert(L::kDyn <= 232448u, "shared memory budget");
+    static_assert(L::kSlots <= kMaxSlots, "K/V ring");
     auto kern = prefill_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
     if (e != cudaSuccess) return e;
