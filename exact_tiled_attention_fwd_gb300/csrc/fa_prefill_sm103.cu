@@ -75,6 +75,7 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kTiles = 2;  // Q tiles per CTA
 constexpr float kRescaleThreshold = 8.0f;
+constexpr float kPBound = 256.0f;  // 2^kRescaleThreshold: the largest P the reference allows
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 64 bf16
@@ -108,7 +109,8 @@ enum BarId : uint32_t {
     B_P_EMPTY = 26,   // + tile: PV^t_j is done (P tile free, O^t current)
     B_O_FINAL = 28,   // + tile
     B_MMA_DONE = 30,  // + tile
-    B_COUNT = 32,
+    B_EXP_TURN = 32,  // + tile: the other tile has finished its exponentials
+    B_COUNT = 34,
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -219,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(bar(B_S_FREE + t), 4);  // one arrive per softmax warp
             mbar_init(bar(B_P_FULL + t), 4);
+            mbar_init(bar(B_EXP_TURN + t), 4);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -397,7 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = quarter * 32 + lane;       // row of the tile == TMEM lane
         const int r0 = row0 + t * kBlockM;
         const int row = r0 + r;                   // row within the sequence
-        const int n_t = nb[t];
+        const int n_t = t == 0 ? nb[0] : nb[1];
+        const int n_other = t == 0 ? nb[1] : nb[0];  // blocks of the other tile
         const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t s_col = t * 128;
         const uint32_t o_col = 256 + t * 128;
@@ -430,37 +434,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < kBlockN; ++i)
                     if (i > lim_c) u[i] = __float_as_uint(NEG_INF);
             }
-            float mx0 = NEG_INF, mx1 = NEG_INF, mx2 = NEG_INF, mx3 = NEG_INF;
-#pragma unroll
-            for (int i = 0; i < kBlockN; i += 8) {
-                mx0 = fmax3(mx0, __uint_as_float(u[i]), __uint_as_float(u[i + 1]));
-                mx1 = fmax3(mx1, __uint_as_float(u[i + 2]), __uint_as_float(u[i + 3]));
-                mx2 = fmax3(mx2, __uint_as_float(u[i + 4]), __uint_as_float(u[i + 5]));
-                mx3 = fmax3(mx3, __uint_as_float(u[i + 6]), __uint_as_float(u[i + 7]));
+            // The two tiles take turns on their exponentials (tile 1 block j
+            // after tile 0 block j, tile 0 block j after tile 1 block j-1), so
+            // the warps of one tile run their exponentials while the other
+            // tile's warps on the same sub-partitions load, store and wait.
+            {
+                const int jo = t == 1 ? j : j - 1;
+                if (jo >= 0 && jo < n_other && !warp_wait(bar(B_EXP_TURN + t), jo & 1, abort_flag, p.err, lim)) {
+                    ok = false;
+                    break;
+                }
             }
-            const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * c;
-            const float m_new = fmaxf(m_ref, m_blk);
-            const bool resc = (m_ref != NEG_INF) && (m_new - m_ref > kRescaleThreshold);
-            const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
-            if (resc || m_ref == NEG_INF) m_ref = m_new;
-            const float mu = (m_ref == NEG_INF) ? 0.f : m_ref;
-            // P = 2^(S c - mu) as bf16 pairs, kept in registers until the P
-            // tile is free, so the wait for the previous P.V overlaps this.
-            const float2 c2 = make_float2(c, c);
-            const float2 nmu2 = make_float2(-mu, -mu);
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            // P = 2^(S c - mu) as bf16 pairs and its row sum, kept in
+            // registers until the P tile is free, so that the wait for the
+            // previous P.V overlaps this work.
             uint32_t pk[kBlockN / 2];
+            float2 acc0, acc1;
+            auto exponentials = [&](float mu) {
+                const float2 c2 = make_float2(c, c);
+                const float2 nmu2 = make_float2(-mu, -mu);
+                acc0 = make_float2(0.f, 0.f);
+                acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < kBlockN / 2; ++i) {
-                const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2, nmu2);
-                const float2 e = make_float2(ex2(x.x), ex2(x.y));
-                if (i & 1)
-                    acc1 = __fadd2_rn(acc1, e);
-                else
-                    acc0 = __fadd2_rn(acc0, e);
-                pk[i] = pack_bf16x2(e.x, e.y);
+                for (int i = 0; i < kBlockN / 2; ++i) {
+                    const float2 x =
+                        __ffma2_rn(make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2, nmu2);
+                    const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                    if (i & 1)
+                        acc1 = __fadd2_rn(acc1, e);
+                    else
+                        acc0 = __fadd2_rn(acc0, e);
+                    pk[i] = pack_bf16x2(e.x, e.y);
+                }
+            };
+            // Usual case: the reference m_ref stands.  P is computed against it
+            // without the row max; since every P is at most the row sum, a sum
+            // of at most 2^kRescaleThreshold shows that no P exceeds the bound
+            // and the block is done.  Otherwise (first block, a jump of the
+            // max, or a sum that is merely large) the row max decides, as
+            // below, and P is recomputed.
+            float alpha = 1.f;
+            bool resc = false;
+            bool exact = m_ref == NEG_INF;
+            if (!exact) {
+                exponentials(m_ref);
+                exact = !(((acc0.x + acc0.y) + (acc1.x + acc1.y)) <= kPBound);  // also catches inf / NaN
+            }
+            if (exact) {
+                float mx0 = NEG_INF, mx1 = NEG_INF, mx2 = NEG_INF, mx3 = NEG_INF;
+#pragma unroll
+                for (int i = 0; i < kBlockN; i += 8) {
+                    mx0 = fmax3(mx0, __uint_as_float(u[i]), __uint_as_float(u[i + 1]));
+                    mx1 = fmax3(mx1, __uint_as_float(u[i + 2]), __uint_as_float(u[i + 3]));
+                    mx2 = fmax3(mx2, __uint_as_float(u[i + 4]), __uint_as_float(u[i + 5]));
+                    mx3 = fmax3(mx3, __uint_as_float(u[i + 6]), __uint_as_float(u[i + 7]));
+                }
+                const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * c;
+                const float m_new = fmaxf(m_ref, m_blk);
+                resc = (m_ref != NEG_INF) && (m_new - m_ref > kRescaleThreshold);
+                alpha = resc ? ex2(m_ref - m_new) : 1.f;
+                if (resc || m_ref == NEG_INF) m_ref = m_new;
+                exponentials(m_ref == NEG_INF ? 0.f : m_ref);
             }
             l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_EXP_TURN + (t ^ 1)));
             // PV^t_{j-1} must be done before the P tile is rewritten or O^t is
             // rescaled.  (PV^t_{j-2} is known done: it was issued before
             // S^t_j.)
