@@ -53,7 +53,7 @@ WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), packe
 # and causal launches; profiles/decode_split_kernel_B16H32d128.md: the
 # 16-sequence capture scaled by cached tokens to the 64-sequence launch).
 # Set to None whenever a kernel changes after its capture.
-PREFILL_TRAFFIC_BYTES = 418.5e6
+PREFILL_TRAFFIC_BYTES = 420.0e6
 DECODE_TRAFFIC_BYTES = 9.29e9
 
 

@@ -113,6 +113,29 @@ def test_large_scores_rescale(fa):
         assert_lse_close(lse, L_ref, f"ramp c{causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("top", [1.1, 0.0, -4.0])
+def test_score_drift(fa, top, d):
+    """Scores that drift along the keys by a set amount per 128-key block.
+
+    top=1.1 raises the row max by about 3 log2 units per block: the row sum
+    often exceeds 2^8 while the max stays within the exponent reference's
+    bound (the exact path without a rescale), and every few blocks the bound
+    is crossed (a rescale).  top=0 gives equal scores (P = 1 against the
+    reference), top=-4 falling scores (later blocks underflow toward 0)."""
+    B, N, H = 1, 1024, 2
+    q = torch.full((B, N, H, d), 16.0 / d, dtype=torch.bfloat16)
+    ramp = torch.linspace(0.0, top, N).reshape(1, N, 1, 1)
+    k = (torch.ones((B, N, H, d)) * ramp).to(torch.bfloat16)
+    v = W.randn_bf16((B, N, H, d), 78)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    for causal in (False, True):
+        o, lse = run_dense(fa, q, k, v, 1.0, causal)
+        O_ref, L_ref = oracle.attention_dense(f64(q), f64(k), f64(v), 1.0, causal)
+        assert_o_close(o, O_ref, f"drift {top} d{d} c{causal}")
+        assert_lse_close(lse, L_ref, f"drift {top} d{d} c{causal}")
+
+
 def test_lse_optional_and_deterministic(fa):
     q, k, v = W.dense_inputs(2, 700, 4, 128, 31, "cuda")
     o1 = torch.empty_like(q)
