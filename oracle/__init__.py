@@ -11,6 +11,8 @@ from .attention import (  # noqa: F401
     attention_dense,
     attention_varlen,
     attention_paged,
+    attention_varlen_paged,
+    store_kvcache,
     gather_paged_kv,
     visible_mask,
 )

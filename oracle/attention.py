@@ -38,6 +38,9 @@ attention_head_blocked   the blocked online-softmax recurrence (invariant
 attention_dense          [B, N, H, d] batched multi-head wrapper
 attention_varlen         packed [total, H, d] + cu_seqlens wrapper
 attention_paged          single-query decode over a paged KV pool
+store_kvcache            scatter of one step's K/V rows into the page pool
+attention_varlen_paged   packed prefill whose K/V are read through the page
+                         table (a chunk that continues a cached prefix)
 gather_paged_kv          host walk of block_table (the bit-exact gather
                          reference)
 
@@ -295,3 +298,64 @@ def attention_paged(q, k_cache, v_cache, block_table, seqlens, page_size: int, s
             lse[b, h] = l[0]
     return O, lse
 
+
+
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping, page_size: int):
+    """Write one step's key/value rows into the paged pool (the store_kvcache
+    step of the dlog.com.cn page, "v3 attention 的一条完整数据流", step 3).
+
+    k, v: [T, H_kv, d]; k_cache, v_cache: [num_pages, page_size, H_kv, d];
+    slot_mapping: [T] ints.  Row i goes to flat slot slot_mapping[i], i.e.
+    page slot // page_size, offset slot % page_size.  A negative slot marks a
+    token that is not stored (padding); the pages leave this open and this is
+    the reading taken.  Returns new arrays; the inputs are not modified.  A
+    pure copy: no arithmetic.
+    """
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    k, v = np.asarray(k), np.asarray(v)
+    for i, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        page, off = divmod(int(slot), page_size)
+        kc[page, off] = k[i]
+        vc[page, off] = v[i]
+    return kc, vc
+
+
+def attention_varlen_paged(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, page_size: int,
+                           scale: float, causal: bool):
+    """Packed variable-length prefill whose keys and values live in the page
+    pool (the prefill entry point with block_table, dlog.com.cn page "v3 实际
+    调用的两个函数": a chunk that continues a cached prefix reads its K/V
+    through block_table).
+
+    q: [total_q, H, d] packed by cu_seqlens_q.  Sequence s has
+    Lk = cu_seqlens_k[s+1] - cu_seqlens_k[s] keys, the logical tokens
+    0 .. Lk-1 of its pages (block_table[s]); its Lq queries are the newest Lq
+    of those tokens, so with causal the bottom-right alignment applies (query
+    i sees keys j <= i + Lk - Lq).  The oracle gathers each sequence's K/V on
+    the host and runs the very routine attention_varlen uses on contiguous
+    K/V, so the two agree exactly on the same rows.
+    Returns O [total_q, H, d] and LSE [H, total_q].
+    """
+    q = _f64(q)
+    cq = [int(x) for x in cu_seqlens_q]
+    ck = [int(x) for x in cu_seqlens_k]
+    total_q, H, d = q.shape
+    Hkv = np.asarray(k_cache).shape[2]
+    g = H // Hkv
+    O = np.zeros_like(q)
+    lse = np.full((H, total_q), -np.inf)
+    for s in range(len(cq) - 1):
+        qs, qe = cq[s], cq[s + 1]
+        Lk = ck[s + 1] - ck[s]
+        if qe == qs:
+            continue
+        kb = _f64(gather_paged_kv(k_cache, block_table[s], Lk, page_size))
+        vb = _f64(gather_paged_kv(v_cache, block_table[s], Lk, page_size))
+        for h in range(H):
+            o, l = attention_head(q[qs:qe, h], kb[:, h // g], vb[:, h // g], scale, causal)
+            O[qs:qe, h] = o
+            lse[h, qs:qe] = l
+    return O, lse
