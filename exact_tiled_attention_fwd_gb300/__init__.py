@@ -30,6 +30,7 @@ FA_ERR_SCRATCH_CAPACITY = 6
 EXPORTS = (
     "fa_abi_version", "fa_status_string", "fa_fwd", "fa_varlen_fwd", "fa_paged_workspace_size",
     "fa_paged_fwd", "fa_paged_fwd_noalloc", "fa_paged_gather", "fa_device_status", "fa_selftest_wait_timeout",
+    "fa_varlen_paged_fwd", "fa_store_kvcache",
 )
 
 _lib = None
@@ -65,6 +66,10 @@ def load(path: str | None = None):
     lib.fa_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_paged_fwd_noalloc.restype = i
     lib.fa_paged_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+    lib.fa_varlen_paged_fwd.restype = i
+    lib.fa_varlen_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, i, f, i, vp]
+    lib.fa_store_kvcache.restype = i
+    lib.fa_store_kvcache.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.fa_paged_gather.restype = i
     lib.fa_paged_gather.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.fa_device_status.restype = i
@@ -115,6 +120,21 @@ def fa_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, max_seq
     return load().fa_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
                                 _ptr(cu_seqlens_k), num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k,
                                 H, Hkv, d, scale, int(bool(causal)), _stream(stream))
+
+
+def fa_varlen_paged_fwd(q, k_cache, v_cache, o, lse, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
+                        max_seqlen_q, max_seqlen_k, total_q, H, Hkv, d, page_size, num_pages, max_pages_per_seq,
+                        scale, causal, stream=None) -> int:
+    return load().fa_varlen_paged_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                                      _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(block_table), num_seqs,
+                                      max_seqlen_q, max_seqlen_k, total_q, H, Hkv, d, page_size, num_pages,
+                                      max_pages_per_seq, scale, int(bool(causal)), _stream(stream))
+
+
+def fa_store_kvcache(k, v, k_cache, v_cache, slot_mapping, num_tokens, Hkv, d, page_size, num_pages,
+                     stream=None) -> int:
+    return load().fa_store_kvcache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), num_tokens,
+                                   Hkv, d, page_size, num_pages, _stream(stream))
 
 
 def fa_paged_workspace_size(B, H, d, max_seqlen) -> int:
@@ -229,4 +249,43 @@ def attention_paged(q, k_cache, v_cache, block_table, seqlens, max_seqlen, scale
     st = fa_paged_fwd(q, k_cache, v_cache, block_table, seqlens, out, lse, B, H, Hkv, d, page_size, num_pages,
                       block_table.shape[1], max_seqlen, scale, causal, workspace, workspace.numel(), stream)
     _check(st, "fa_paged_fwd")
+    return out, lse
+
+
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """Write this step's rows into the page pool.  k, v: [T, Hkv, d] bf16;
+    caches: [num_pages, page_size, Hkv, d] bf16; slot_mapping: int32 [T]
+    (flat slots, negative = skip).  Modifies the caches in place."""
+    import torch
+
+    for name, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _req(t, name, torch.bfloat16)
+    _req(slot_mapping, "slot_mapping", torch.int32)
+    T, Hkv, d = k.shape
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    st = fa_store_kvcache(k, v, k_cache, v_cache, slot_mapping, T, Hkv, d, page_size, num_pages, stream)
+    _check(st, "fa_store_kvcache")
+
+
+def attention_varlen_paged(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, max_seqlen_q,
+                           max_seqlen_k, scale=None, causal=True, out=None, lse=None, stream=None):
+    """Packed varlen prefill reading K/V through a page table (a chunk that
+    continues a cached prefix).  q: [total_q, H, d]; caches: [num_pages, 16,
+    Hkv, d] bf16; cu_seqlens_q/k: int32 [num_seqs + 1]; block_table: int32
+    [num_seqs, max_pages].  Returns (O [total_q, H, d], LSE [H, total_q])."""
+    import torch
+
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _req(t, name, torch.bfloat16)
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k), ("block_table", block_table)):
+        _req(t, name, torch.int32)
+    total_q, H, d = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = fa_varlen_paged_fwd(q, k_cache, v_cache, out, lse, cu_seqlens_q, cu_seqlens_k, block_table,
+                             cu_seqlens_q.numel() - 1, max_seqlen_q, max_seqlen_k, total_q, H, Hkv, d, page_size,
+                             num_pages, block_table.shape[1], scale, causal, stream)
+    _check(st, "fa_varlen_paged_fwd")
     return out, lse

@@ -17,7 +17,7 @@ __device__ unsigned int g_fa_error_word;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr int kMaxDevices = 64;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -68,11 +68,13 @@ fa_status ensure_init(unsigned int** err_out) {
 }
 
 // 3-D view (d, heads, rows) of a [rows, heads, d] bf16 tensor; a box is 64
-// elements of d (128 bytes, the swizzle span) x 1 head x 128 rows.
-fa_status make_map(CUtensorMap* map, const void* base, int d, int heads, long long rows) {
+// elements of d (128 bytes, the swizzle span) x 1 head x box_rows rows (a
+// 128-row tile, or one 16-token page of the paged pool).
+fa_status make_map(CUtensorMap* map, const void* base, int d, int heads, long long rows,
+                   int box_rows = fa::kBlockM) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
-    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(fa::kBlockM)};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -186,6 +188,88 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
     p.wait_limit_ns = wait_limit_ns();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
+}
+
+int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, const int* block_table, int num_seqs,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int H, int Hkv, int d, int page_size,
+                        int num_pages, int max_pages_per_seq, float scale, int causal, void* stream) {
+    if (!q || !k_cache || !v_cache || !o || !cu_seqlens_q || !cu_seqlens_k || !block_table) return FA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u))
+        return FA_ERR_INVALID;
+    if (num_seqs < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || total_q < 1 || max_seqlen_q < 1 || max_seqlen_k < 1 ||
+        num_pages < 1 || max_pages_per_seq < 1 || !scale_ok(scale))
+        return FA_ERR_INVALID;
+    if (static_cast<long long>(max_pages_per_seq) * page_size < max_seqlen_k) return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (page_size != fa::kPageSize) return FA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
+    // rows of the pool view, plus one page of zero fill past its end, must be
+    // addressable by a 32-bit TMA coordinate
+    if ((static_cast<long long>(num_pages) + 1) * page_size > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    const long long pool_rows = static_cast<long long>(num_pages) * page_size;
+    CUtensorMap tq, tk, tv;
+    if ((st = make_map(&tq, q, d, H, total_q)) != FA_OK) return st;
+    if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, fa::kPageSize)) != FA_OK) return st;
+    if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, fa::kPageSize)) != FA_OK) return st;
+    fa::PrefillParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.N = 0;
+    p.num_seqs = num_seqs;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
+    p.max_seqlen_q = max_seqlen_q;
+    p.max_seqlen_k = max_seqlen_k;
+    p.total_q = total_q;
+    p.total_k = 0;  // not used with a page table
+    p.num_q_blocks = (max_seqlen_q + fa::kBlockM - 1) / fa::kBlockM;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.lse_head_stride = total_q;
+    p.err = err;
+    p.wait_limit_ns = wait_limit_ns();
+    p.block_table = block_table;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
+}
+
+int fa_store_kvcache(const void* k, const void* v, void* k_cache, void* v_cache, const int* slot_mapping,
+                     int num_tokens, int Hkv, int d, int page_size, int num_pages, void* stream) {
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return FA_ERR_INVALID;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return FA_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(slot_mapping) & 3u) return FA_ERR_INVALID;
+    if (num_tokens < 0 || Hkv < 1 || num_pages < 1 || page_size < 1) return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const long long num_slots = static_cast<long long>(num_pages) * page_size;
+    if (num_slots > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (num_tokens == 0) return finish(cudaSuccess, s);
+    fa::StoreParams p{};
+    p.k = k;
+    p.v = v;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.slot_mapping = slot_mapping;
+    p.T = num_tokens;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.num_slots = num_slots;
+    p.err = err;
+    return finish(fa::launch_store_kvcache(p, s), s);
 }
 
 size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen) {

@@ -255,6 +255,38 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
     }
 }
 
+// store_kvcache: row i of this step's K and V goes to flat slot
+// slot_mapping[i] of the page pool (page slot / page_size, offset
+// slot % page_size, so with contiguous pages the slot is the row of the pool
+// viewed as [num_pages * page_size, Hkv, d]).  A negative slot is skipped; a
+// slot past the pool is skipped and reported.  Work is spread over 16-byte
+// chunks, one chunk of K and the same chunk of V per thread and step.
+__global__ void __launch_bounds__(256) store_kvcache_kernel(const StoreParams p) {
+    const int chunks = p.Hkv * p.d / 8;
+    const long long units = static_cast<long long>(p.T) * chunks;
+    const uint16_t* ks = static_cast<const uint16_t*>(p.k);
+    const uint16_t* vs = static_cast<const uint16_t*>(p.v);
+    uint16_t* kd = static_cast<uint16_t*>(p.k_cache);
+    uint16_t* vd = static_cast<uint16_t*>(p.v_cache);
+    for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
+         u += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long t = u / chunks;
+        const int c = static_cast<int>(u % chunks);
+        const int slot = __ldg(p.slot_mapping + t);
+        if (slot < 0) continue;
+        if (slot >= p.num_slots) {
+            if (c == 0) atomicOr(p.err, FA_DEVERR_INDEX);
+            continue;
+        }
+        const size_t src = static_cast<size_t>(t) * chunks * 8 + static_cast<size_t>(c) * 8;
+        const size_t dst = static_cast<size_t>(slot) * chunks * 8 + static_cast<size_t>(c) * 8;
+        const uint4 kv = ldg_stream(ks + src);
+        const uint4 vv = ldg_stream(vs + src);
+        *reinterpret_cast<uint4*>(kd + dst) = kv;
+        *reinterpret_cast<uint4*>(vd + dst) = vv;
+    }
+}
+
 // One CTA waits on a barrier nothing arrives on; the bounded wait must give
 // up and record the timeout.
 __global__ void wait_selftest_kernel(unsigned int* err, unsigned long long limit_ns) {
@@ -292,6 +324,14 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream) {
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
     dim3 grid((p.max_seqlen + kPageSize - 1) / kPageSize, p.B);
     gather_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_store_kvcache(const StoreParams& p, cudaStream_t stream) {
+    const long long units = static_cast<long long>(p.T) * (p.Hkv * p.d / 8);
+    const long long want = (units + 255) / 256;
+    const int grid = static_cast<int>(want < 152 * 16 ? want : 152 * 16);
+    store_kvcache_kernel<<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -34,6 +34,13 @@ struct PrefillParams {
     long long lse_head_stride;  // N (dense, [B,H,N]) or total_q (varlen, [H,total])
     unsigned int* err;       // device error word
     unsigned long long wait_limit_ns;
+    // Paged K/V (varlen only): when block_table is set, sequence s's keys are
+    // the logical tokens 0 .. Lk-1 of its pages, token t at page
+    // block_table[s * max_pages + t / kPageSize], slot t % kPageSize, and the
+    // K/V tensor maps view the pool [num_pages * kPageSize, Hkv, d] with
+    // kPageSize-row boxes.
+    const int* block_table;
+    int max_pages, num_pages;
 };
 
 struct DecodeParams {
@@ -70,6 +77,18 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream);
+
+struct StoreParams {
+    const void* k;           // bf16 [T, Hkv, d]
+    const void* v;
+    void* k_cache;           // bf16 [num_pages * page_size, Hkv, d]
+    void* v_cache;
+    const int* slot_mapping; // int32 [T]
+    int T, Hkv, d;
+    long long num_slots;     // num_pages * page_size
+    unsigned int* err;
+};
+cudaError_t launch_store_kvcache(const StoreParams& p, cudaStream_t stream);
 
 // Size of the fixed device scratch used by fa_paged_fwd_noalloc, and the
 // per-device lookup of its address (first call on a device does the lookup).

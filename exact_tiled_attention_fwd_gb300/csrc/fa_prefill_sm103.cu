@@ -110,7 +110,8 @@ enum BarId : uint32_t {
     B_O_FINAL = 28,   // + tile
     B_MMA_DONE = 30,  // + tile
     B_EXP_TURN = 32,  // + tile: the other tile has finished its exponentials
-    B_COUNT = 34,
+    B_V_TAIL = 34,    // paged: stale rows of the last V tile are zeroed
+    B_COUNT = 35,
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -177,8 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         Lq = p.cu_q[seq + 1] - q_start;
         k_start = p.cu_k[seq];
         Lk = p.cu_k[seq + 1] - k_start;
-        const bool bad = q_start < 0 || Lq < 0 || k_start < 0 || Lk < 0 || q_start + Lq > p.total_q ||
-                         k_start + Lk > p.total_k || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k;
+        const bool bad = q_start < 0 || Lq < 0 || Lk < 0 || q_start + Lq > p.total_q || Lq > p.max_seqlen_q ||
+                         Lk > p.max_seqlen_k ||
+                         (p.block_table != nullptr ? Lk > p.max_pages * kPageSize
+                                                   : (k_start < 0 || k_start + Lk > p.total_k));
         if (bad) {
             if (threadIdx.x == 0 && qb == 0) atomicOr(p.err, FA_DEVERR_INDEX);
             return;
@@ -199,6 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         nb[t] = tile_blocks<CAUSAL>(row0 + t * kBlockM, r_last[t], Lk, diag);
     }
     const int nmax = max(nb[0], nb[1]);
+    // Paged keys whose last page is only partly used: the stale slots past Lk
+    // are loaded with the page, and their V rows are zeroed before the last
+    // P.V (P is 0 there, but 0 * a non-finite stale value would not be).
+    const bool v_tail = p.block_table != nullptr && (Lk % kPageSize) != 0 && nmax > 0 &&
+                        (Lk - 1) / kBlockN == nmax - 1;
     const long long lse_base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
@@ -279,10 +287,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) return;
                     mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kTile);
                     const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+                    const uint32_t dst = sbase + L::kKV + s * L::kTile;
+                    if (p.block_table == nullptr) {
 #pragma unroll
-                    for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + L::kKV + s * L::kTile + pn * kPanelBytes, map, bar(B_KV_FULL + s), pn * 64, hk,
-                                    k_start + j * kBlockN);
+                        for (int pn = 0; pn < kPanels; ++pn)
+                            tma_load_3d(dst + pn * kPanelBytes, map, bar(B_KV_FULL + s), pn * 64, hk, k_start + j * kBlockN);
+                    } else {
+                        // One box per page.  A page past the sequence, or a bad
+                        // table entry, is loaded from just past the pool: TMA
+                        // fills zeros there (and still counts the bytes).
+                        const int* bt = p.block_table + static_cast<size_t>(seq) * p.max_pages;
+#pragma unroll 1
+                        for (int pg = 0; pg < kBlockN / kPageSize; ++pg) {
+                            const int tok0 = j * kBlockN + pg * kPageSize;
+                            int row = p.num_pages * kPageSize;
+                            if (tok0 < Lk) {
+                                const int page = bt[tok0 / kPageSize];
+                                if (page >= 0 && page < p.num_pages)
+                                    row = page * kPageSize;
+                                else
+                                    atomicOr(p.err, FA_DEVERR_INDEX);
+                            }
+#pragma unroll
+                            for (int pn = 0; pn < kPanels; ++pn)
+                                tma_load_3d(dst + pn * kPanelBytes + pg * kPageSize * 128, map, bar(B_KV_FULL + s), pn * 64,
+                                            hk, row);
+                        }
+                    }
                     last_fill[s] = i / kSlots;
 #pragma unroll
                     for (int t = 0; t < kTiles; ++t) {
@@ -309,6 +340,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (nb[t] > 0) mbar_wait_drain(bar(B_Q_FULL + t), 0, lim);
             }
             __syncwarp();
+            if (v_tail) {
+                // The whole warp zeroes rows [Lk, roundup(Lk, page)) of the
+                // last V tile once it has landed, then releases the last P.V.
+                const int i_last = pos_v(nmax - 1, nmax);
+                if (warp_wait(bar(B_KV_FULL + i_last % kSlots), (i_last / kSlots) & 1, abort_flag, p.err, lim)) {
+                    const int kb = (nmax - 1) * kBlockN;
+                    const int r_lo = Lk - kb;
+                    const int r_hi = ((Lk + kPageSize - 1) / kPageSize) * kPageSize - kb;
+                    const uint32_t base = sbase + L::kKV + (i_last % kSlots) * L::kTile;
+                    for (int e = lane; e < (r_hi - r_lo) * kPanels * 8; e += 32) {
+                        const int chunk = e & 7;
+                        const int pn = (e >> 3) % kPanels;
+                        const int r = r_lo + (e >> 3) / kPanels;
+                        st_shared_v4(base + pn * kPanelBytes + r * 128 + chunk * 16, 0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_V_TAIL));
+                }
+            }
         } else if (warp == 1 || warp == 2) {
             // ================= MMA issuers (warp 1: tile 0, warp 2: tile 1) =================
             const int t = warp - 1;
@@ -371,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ok = ok && warp_wait(bar(B_P_FULL + t), j & 1, abort_flag, p.err, lim);
                     wait_item(pos_v(j, nmax));
+                    if (v_tail && j == nmax - 1) ok = ok && warp_wait(bar(B_V_TAIL), 0, abort_flag, p.err, lim);
                     if (!ok) break;
                     issue_pv(j);
                 }

@@ -154,3 +154,55 @@ def c4_lengths(seed: int = 1238) -> list[int]:
 
 def c5_lengths(seed: int = 1239) -> list[int]:
     return uniform_lengths(PAGED_C5["B"], PAGED_C5["lo"], PAGED_C5["hi"], seed)
+
+
+@dataclass
+class ChunkBatch:
+    q: torch.Tensor            # [total_q, H, d], the newest tokens of each sequence
+    k_cache: torch.Tensor      # [num_pages, 16, Hkv, d]
+    v_cache: torch.Tensor
+    block_table: torch.Tensor  # int32 [S, max_pages]
+    cu_q: torch.Tensor         # int32 [S + 1]
+    cu_k: torch.Tensor         # int32 [S + 1]
+    lengths_q: list
+    lengths_k: list
+    max_q: int
+    max_k: int
+    num_pages: int
+
+
+def chunk_inputs(lengths_q, lengths_k, H, d, seed: int, device="cpu", Hkv=None, page_size=PAGE_SIZE,
+                 slack_pages=0, stale=float("nan"), pool_on_device=False) -> ChunkBatch:
+    """A prefill chunk that continues cached prefixes: sequence s has
+    lengths_k[s] keys in the page pool (pages in a seeded random permutation)
+    and its lengths_q[s] newest tokens as queries.  Every slot no sequence
+    uses (the tail of each last page, the slack pages) holds ``stale``."""
+    Hkv = H if Hkv is None else Hkv
+    S = len(lengths_k)
+    pages_per = [(L + page_size - 1) // page_size for L in lengths_k]
+    num_pages = max(1, sum(pages_per) + slack_pages)
+    perm = torch.randperm(num_pages, generator=_gen(seed * 11 + 5)).to(torch.int32)
+    maxp = max(1, max(pages_per))
+    bt = torch.full((S, maxp), -1, dtype=torch.int32)
+    used = torch.zeros((num_pages, page_size), dtype=torch.bool)
+    pos = 0
+    for s, n in enumerate(pages_per):
+        bt[s, :n] = perm[pos:pos + n]
+        pos += n
+        for t in range(0, lengths_k[s], page_size):
+            used[int(bt[s, t // page_size]), : min(page_size, lengths_k[s] - t)] = True
+    shape = (num_pages, page_size, Hkv, d)
+    if pool_on_device:
+        kc = randn_bf16_device(shape, seed * 11 + 1, device)
+        vc = randn_bf16_device(shape, seed * 11 + 2, device)
+    else:
+        kc = randn_bf16(shape, seed * 11 + 1, device)
+        vc = randn_bf16(shape, seed * 11 + 2, device)
+    if stale is not None:
+        mask = (~used).to(kc.device)
+        kc[mask] = stale
+        vc[mask] = stale
+    cq, ck = cu_seqlens(lengths_q), cu_seqlens(lengths_k)
+    q = randn_bf16((int(cq[-1]), H, d), seed * 11 + 0, device)
+    return ChunkBatch(q, kc, vc, bt.to(device), cq.to(device), ck.to(device), list(lengths_q), list(lengths_k),
+                      max(lengths_q), max(lengths_k), num_pages)

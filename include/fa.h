@@ -104,6 +104,52 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
                   int H, int Hkv, int d, float scale, int causal, void* stream);
 
 /*
+ * Packed variable-length prefill whose keys and values are read through a
+ * page table (the prefill entry point with block_table of the dlog.com.cn
+ * page, "v3 实际调用的两个函数": a chunk that continues a cached prefix reads
+ * its K/V straight from the page pool).
+ *   q, o : [total_q, H, d] bf16, packed by cu_seqlens_q as in fa_varlen_fwd
+ *   k_cache, v_cache : [num_pages, page_size, Hkv, d] bf16, the whole pool
+ *   cu_seqlens_q, cu_seqlens_k : int32 [num_seqs + 1], DEVICE.  Sequence s
+ *       has Lq = cu_q[s+1] - cu_q[s] queries and Lk = cu_k[s+1] - cu_k[s]
+ *       keys; its keys are the logical tokens 0 .. Lk-1 of its pages and its
+ *       queries are the newest Lq of them, so with causal = 1 query i sees
+ *       keys j <= i + Lk - Lq (bottom-right; Lq <= Lk is expected).
+ *   block_table : int32 [num_seqs, max_pages_per_seq], DEVICE; token t of
+ *       sequence s is page block_table[s][t / page_size], slot
+ *       t % page_size.  Entries past ceil(Lk / page_size) are never read; an
+ *       entry outside [0, num_pages) is treated as a page of zeros and
+ *       reported as FA_ERR_DEVICE_INDEX.  Slots of a sequence's last page
+ *       past Lk may hold anything (they are never used, even if not finite).
+ *   max_seqlen_q, max_seqlen_k : bounds as in fa_varlen_fwd;
+ *       max_pages_per_seq * page_size >= max_seqlen_k.
+ *   lse : [H, total_q] fp32, may be NULL.
+ * page_size must be 16.
+ */
+int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, const int* block_table,
+                        int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q,
+                        int H, int Hkv, int d, int page_size, int num_pages,
+                        int max_pages_per_seq, float scale, int causal, void* stream);
+
+/*
+ * Write one step's key/value rows into the page pool (the store_kvcache step
+ * of the dlog.com.cn page, "v3 attention 的一条完整数据流", step 3, which runs
+ * before the attention call of the same step).
+ *   k, v : [num_tokens, Hkv, d] bf16
+ *   k_cache, v_cache : [num_pages, page_size, Hkv, d] bf16, modified in place
+ *   slot_mapping : int32 [num_tokens], DEVICE; row i goes to flat slot
+ *       slot_mapping[i], i.e. page slot / page_size, offset
+ *       slot % page_size.  A negative slot means "do not store" (padding);
+ *       a slot >= num_pages * page_size is skipped and reported as
+ *       FA_ERR_DEVICE_INDEX.  Two rows with the same slot: one of them wins.
+ * num_tokens may be 0 (nothing is launched).  Any page_size >= 1.
+ */
+int fa_store_kvcache(const void* k, const void* v, void* k_cache, void* v_cache,
+                     const int* slot_mapping, int num_tokens, int Hkv, int d,
+                     int page_size, int num_pages, void* stream);
+
+/*
  * Bytes of device workspace fa_paged_fwd needs for these sizes (the split-KV
  * partial results).  Returns 0 for invalid sizes.
  */

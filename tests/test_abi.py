@@ -51,7 +51,7 @@ def test_status_strings(lib):
     for code in range(6):
         assert lib.status_string(code).startswith("FA_")
     assert "unknown" in lib.status_string(99)
-    assert lib.fa_abi_version() == 1
+    assert lib.fa_abi_version() == 2
 
 
 def test_validation_without_gpu(lib):
@@ -83,6 +83,21 @@ def test_validation_without_gpu(lib):
     assert lib.fa_paged_fwd(A, A, A, 0, A, A, None, 2, 4, 4, 128, 16, 10, 8, 100, 0.1, 1, A, ws, S) == \
         lib.FA_ERR_INVALID
     assert lib.fa_selftest_wait_timeout(0, S) == lib.FA_ERR_INVALID
+    # paged varlen prefill: null table, unaligned cu_seqlens, page size, too
+    # few pages per sequence for max_seqlen_k, d
+    vp = lib.fa_varlen_paged_fwd
+    assert vp(A, A, A, A, None, A, A, 0, 2, 64, 200, 64, 4, 2, 128, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_INVALID
+    assert vp(A, A, A, A, None, A + 2, A, A, 2, 64, 200, 64, 4, 2, 128, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_INVALID
+    assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 128, 32, 30, 13, 0.1, 1, S) == lib.FA_ERR_UNSUPPORTED
+    assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 128, 16, 30, 12, 0.1, 1, S) == lib.FA_ERR_INVALID
+    assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 3, 128, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_INVALID
+    assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 96, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_UNSUPPORTED
+    # store_kvcache: null slot map, unaligned cache, negative token count, d
+    sk = lib.fa_store_kvcache
+    assert sk(A, A, A, A, 0, 8, 2, 128, 16, 4, S) == lib.FA_ERR_INVALID
+    assert sk(A, A, A + 8, A, A, 8, 2, 128, 16, 4, S) == lib.FA_ERR_INVALID
+    assert sk(A, A, A, A, A, -1, 2, 128, 16, 4, S) == lib.FA_ERR_INVALID
+    assert sk(A, A, A, A, A, 8, 2, 96, 16, 4, S) == lib.FA_ERR_UNSUPPORTED
 
 
 def test_workspace_size_monotone(lib):
