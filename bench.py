@@ -45,9 +45,13 @@ C5 = dict(B=64, H=32, d=128)
 SEED_C3 = 1236
 SEED_C4 = 1238
 SEED_C5 = 1239
+SEED_CHUNK = 1240
 WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), packed varlen prefill 16 x U[128,4096] "
             "tokens H32 d64 causal (fa_varlen_fwd), then paged decode B64 H32 d128, KV lengths uniform in "
-            "[512,16384], 16-token pages in a seeded random permutation (fa_paged_fwd)")
+            "[512,16384], 16-token pages in a seeded random permutation (fa_paged_fwd); then a prefix-cache "
+            "continuation chunk, 16 sequences with cached context U[512,8192] + new tokens U[256,2048], H32 d128 "
+            "causal: store the new K/V (fa_store_kvcache), attend through the page table (fa_varlen_paged_fwd), "
+            "and the same shapes with contiguous K/V (fa_varlen_fwd) for comparison")
 # DRAM bytes (read + write) per launch from ncu captures of the current
 # kernels (profiles/prefill_kernel_B1H32N8192d128.md: mean of the non-causal
 # and causal launches; profiles/decode_split_kernel_B16H32d128.md: the
@@ -256,6 +260,7 @@ def ours(args, world, rank, local):
     do_prefill = args.case in ("all", "prefill")
     do_varlen = args.case in ("all", "varlen")
     do_decode = args.case in ("all", "decode")
+    do_chunk = args.case in ("all", "chunk")
     q, k, v = W.dense_inputs(B, N, H, d, SEED_C3, dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -273,6 +278,27 @@ def ours(args, world, rank, local):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     maxp = pb.block_table.shape[1]
+    # prefix-cache continuation: store this chunk's K/V, then attend through
+    # the page table; the same shapes through the contiguous varlen call are
+    # timed beside it (the cost of paging)
+    cl_q, cl_k = W.chunk_lengths(SEED_CHUNK) if do_chunk else ([16], [16])
+    cH, cd = W.CHUNK["H"], W.CHUNK["d"]
+    cb = W.chunk_inputs(cl_q, cl_k, cH, cd, SEED_CHUNK, dev, stale=0.0, pool_on_device=True)
+    c_tq = int(cb.cu_q[-1])
+    co = torch.empty((c_tq, cH, cd), dtype=torch.bfloat16, device=dev)
+    clse = torch.empty((cH, c_tq), dtype=torch.float32, device=dev)
+    cbt_h = cb.block_table.cpu()
+    new_k = W.randn_bf16_device((c_tq, cH, cd), SEED_CHUNK * 5 + 1, dev)
+    new_v = W.randn_bf16_device((c_tq, cH, cd), SEED_CHUNK * 5 + 2, dev)
+    slots = []
+    for s_, (lq_, lk_) in enumerate(zip(cl_q, cl_k)):
+        slots += [int(cbt_h[s_, t // 16]) * 16 + t % 16 for t in range(lk_ - lq_, lk_)]
+    c_slots = torch.tensor(slots, dtype=torch.int32, device=dev)
+    # contiguous copies of every sequence's keys for the comparison leg
+    ck_rows = torch.tensor([int(cbt_h[s_, t // 16]) * 16 + t % 16 for s_, lk_ in enumerate(cl_k) for t in range(lk_)],
+                           dtype=torch.int64, device=dev)
+    c_kc = cb.k_cache.view(-1, cH, cd)[ck_rows].contiguous()
+    c_vc = cb.v_cache.view(-1, cH, cd)[ck_rows].contiguous()
 
     def prefill(causal):
         if not do_prefill:
@@ -297,19 +323,46 @@ def ours(args, world, rank, local):
         if st != F.FA_OK:
             raise F.FAError(st, "fa_paged_fwd")
 
+    def store():
+        if not do_chunk:
+            return
+        st = F.fa_store_kvcache(new_k, new_v, cb.k_cache, cb.v_cache, c_slots, c_tq, cH, cd, 16, cb.num_pages, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_store_kvcache")
+
+    def chunk():
+        if not do_chunk:
+            return
+        st = F.fa_varlen_paged_fwd(cb.q, cb.k_cache, cb.v_cache, co, clse, cb.cu_q, cb.cu_k, cb.block_table,
+                                   len(cl_q), cb.max_q, cb.max_k, c_tq, cH, cH, cd, 16, cb.num_pages,
+                                   cb.block_table.shape[1], 1.0 / math.sqrt(cd), True, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_varlen_paged_fwd")
+
+    def chunk_contiguous():
+        if not do_chunk:
+            return
+        st = F.fa_varlen_fwd(cb.q, c_kc, c_vc, co, clse, cb.cu_q, cb.cu_k, len(cl_q), cb.max_q, cb.max_k, c_tq,
+                             c_kc.shape[0], cH, cH, cd, 1.0 / math.sqrt(cd), True, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_varlen_fwd (contiguous chunk)")
+
     for _ in range(args.warmup):
         flush.zero_()
         prefill(False)
         prefill(True)
         varlen()
         decode()
+        store()
+        chunk()
+        chunk_contiguous()
     torch.cuda.synchronize()
     st = F.fa_device_status(sp)
     if st != F.FA_OK:
         raise F.FAError(st, "warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(K)]
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -328,6 +381,12 @@ def ours(args, world, rank, local):
         e[3].record(stream)
         decode()
         e[4].record(stream)
+        store()
+        e[5].record(stream)
+        chunk()
+        e[6].record(stream)
+        chunk_contiguous()
+        e[7].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
@@ -340,7 +399,15 @@ def ours(args, world, rank, local):
     t_c = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     t_var = sum(e[2].elapsed_time(e[3]) for e in ev) / K
     t_dec = sum(e[3].elapsed_time(e[4]) for e in ev) / K
-    t_nc, t_c, t_var, t_dec = (max_over_ranks(world, x) for x in (t_nc, t_c, t_var, t_dec))
+    t_store = sum(e[4].elapsed_time(e[5]) for e in ev) / K
+    t_chunk = sum(e[5].elapsed_time(e[6]) for e in ev) / K
+    t_chunk_c = sum(e[6].elapsed_time(e[7]) for e in ev) / K
+    t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c = (
+        max_over_ranks(world, x) for x in (t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c))
+    # continuation FLOPs, causal bottom-right, halved-square convention of
+    # the varlen leg: 4 d H (Lq (Lk - Lq) + Lq^2 / 2) per sequence
+    f_chunk = sum(4.0 * cd * cH * (lq_ * (lk_ - lq_) + lq_ * lq_ / 2) for lq_, lk_ in zip(cl_q, cl_k))
+    store_bytes = 2.0 * 2 * c_tq * cH * cd * 2 + c_tq * 4  # K and V read + written, slot map
     f_var = sum(4.0 * L * L * vd * vH / 2 for L in vl)
     var_tflops = f_var / (t_var * 1e-3) / 1e12 if do_varlen else None
     f_nc = prefill_flops(N, d, H, B, False)
@@ -355,7 +422,11 @@ def ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps({"case": args.case, "prefill_ms": [t_nc, t_c], "varlen_ms": t_var, "decode_ms": t_dec,
                               "prefill_tflops": tflops if do_prefill else None, "varlen_tflops": var_tflops,
-                              "decode_gbs": gbs if do_decode else None}), flush=True)
+                              "decode_gbs": gbs if do_decode else None,
+                              "chunk_ms": [t_store, t_chunk, t_chunk_c],
+                              "chunk_tflops": f_chunk / (t_chunk * 1e-3) / 1e12 if do_chunk else None,
+                              "chunk_contiguous_tflops": f_chunk / (t_chunk_c * 1e-3) / 1e12 if do_chunk else None,
+                              "store_gbs": store_bytes / (t_store * 1e-3) / 1e9 if do_chunk else None}), flush=True)
         return
 
     # ---- end to end through the public API with pinned host buffers
@@ -405,7 +476,7 @@ def ours(args, world, rank, local):
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": t_nc + t_c + t_var + t_dec,
+        "ms_per_step": t_nc + t_c + t_var + t_dec + t_store + t_chunk + t_chunk_c,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -421,6 +492,12 @@ def ours(args, world, rank, local):
             "varlen_causal_d64": {"ms": t_var, "tflops": var_tflops, "frac_bf16_peak": var_tflops / peak_tf,
                                   "tokens": int(sum(vl))},
             "paged_decode": {"ms": t_dec, "gbs": gbs, "frac_hbm": gbs / peak_gbs, "kv_tokens": int(sum(lens))},
+            "store_kvcache": {"ms": t_store, "gbs": store_bytes / (t_store * 1e-3) / 1e9,
+                              "frac_hbm": store_bytes / (t_store * 1e-3) / 1e9 / peak_gbs, "tokens": c_tq},
+            "paged_prefill_chunk": {"ms": t_chunk, "tflops": f_chunk / (t_chunk * 1e-3) / 1e12,
+                                    "frac_bf16_peak": f_chunk / (t_chunk * 1e-3) / 1e12 / peak_tf,
+                                    "new_tokens": c_tq, "cached_plus_new_tokens": int(sum(cl_k))},
+            "same_chunk_contiguous_kv": {"ms": t_chunk_c, "tflops": f_chunk / (t_chunk_c * 1e-3) / 1e12},
         },
         "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": tflops / peak_tf, "traffic": PREFILL_TRAFFIC_BYTES,
@@ -430,7 +507,7 @@ def ours(args, world, rank, local):
                             "traffic": DECODE_TRAFFIC_BYTES, "peak_source": f"{peak_src} HBM copy"},
         "e2e": {"value": e2e_tflops * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "prefill legs with q,k,v copied from pinned host memory and O, LSE copied back each step"},
-        "gpu_launches": 5 * K,
+        "gpu_launches": 8 * K,
         "clocks": clk,
         "wall_s_timed": wall,
     }
@@ -447,7 +524,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode"], default="all",
+    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode", "chunk"], default="all",
                     help="run only one leg (for profiling); prints a short line instead of the bench line")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences of the decode leg (profiling)")
     args = ap.parse_args()

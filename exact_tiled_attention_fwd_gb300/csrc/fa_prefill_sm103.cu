@@ -142,7 +142,7 @@ __device__ __forceinline__ int tile_blocks(int r0, int r_last, int Lk, int diag)
     return n;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -180,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Lk = p.cu_k[seq + 1] - k_start;
         const bool bad = q_start < 0 || Lq < 0 || Lk < 0 || q_start + Lq > p.total_q || Lq > p.max_seqlen_q ||
                          Lk > p.max_seqlen_k ||
-                         (p.block_table != nullptr ? Lk > p.max_pages * kPageSize
-                                                   : (k_start < 0 || k_start + Lk > p.total_k));
+                         (PAGED ? Lk > p.max_pages * kPageSize : (k_start < 0 || k_start + Lk > p.total_k));
         if (bad) {
             if (threadIdx.x == 0 && qb == 0) atomicOr(p.err, FA_DEVERR_INDEX);
             return;
@@ -205,8 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Paged keys whose last page is only partly used: the stale slots past Lk
     // are loaded with the page, and their V rows are zeroed before the last
     // P.V (P is 0 there, but 0 * a non-finite stale value would not be).
-    const bool v_tail = p.block_table != nullptr && (Lk % kPageSize) != 0 && nmax > 0 &&
-                        (Lk - 1) / kBlockN == nmax - 1;
+    const bool v_tail = PAGED && (Lk % kPageSize) != 0 && nmax > 0 && (Lk - 1) / kBlockN == nmax - 1;
     const long long lse_base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
@@ -268,70 +266,119 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sbase + L::kQ + t * L::kTile + pn * kPanelBytes, &tm_q, bar(B_Q_FULL + t), pn * 64,
                                     h, q_start + row0 + t * kBlockM);
                 }
-                // Per (tile, slot): whether the tile reads the slot's current
-                // occupant, and the parity of how many occupants it has read.
-                uint32_t used = 0, par = 0;  // bit t * kMaxSlots + slot
-                int last_fill[kMaxSlots];
+            }
+            // Per (tile, slot): whether the tile reads the slot's current
+            // occupant, and the parity of how many occupants it has read.
+            uint32_t used = 0, par = 0;  // bit t * kMaxSlots + slot
+            int last_fill[kMaxSlots];
 #pragma unroll
-                for (int s = 0; s < kMaxSlots; ++s) last_fill[s] = -1;
+            for (int s = 0; s < kMaxSlots; ++s) last_fill[s] = -1;
+            auto account = [&](int i, int j) {
+                const int s = i % kSlots;
+                last_fill[s] = i / kSlots;
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t) {
+                    const uint32_t bit = 1u << (t * kMaxSlots + s);
+                    if (j < nb[t]) {
+                        used |= bit;
+                        par ^= bit;
+                    } else {
+                        used &= ~bit;
+                    }
+                }
+            };
+            if constexpr (!PAGED) {
+                // Contiguous K/V: lane 0 runs the loop, two boxes per tile.
+                if (lane == 0) {
+                    bool ok = true;
+                    auto load = [&](int i, bool is_k, int j) {
+                        const int s = i % kSlots;
+#pragma unroll
+                        for (int t = 0; t < kTiles; ++t) {
+                            const uint32_t bit = 1u << (t * kMaxSlots + s);
+                            if (ok && (used & bit))  // wait until tile t released the previous occupant
+                                ok = mbar_wait(bar(B_KV_EMPTY + t * kMaxSlots + s), ((par & bit) ? 0u : 1u),
+                                               abort_flag, p.err, lim);
+                        }
+                        if (!ok) return;
+                        mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kTile);
+                        const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+#pragma unroll
+                        for (int pn = 0; pn < kPanels; ++pn)
+                            tma_load_3d(sbase + L::kKV + s * L::kTile + pn * kPanelBytes, map, bar(B_KV_FULL + s),
+                                        pn * 64, hk, k_start + j * kBlockN);
+                        account(i, j);
+                    };
+                    load(pos_k(0), true, 0);
+                    for (int j = 0; ok && j < nmax; ++j) {
+                        if (j + 1 < nmax) load(pos_k(j + 1), true, j + 1);
+                        load(pos_v(j, nmax), false, j);
+                    }
+                }
+            } else {
+                // Paged K/V: the whole warp runs the loop (its waits are
+                // warp-uniform); lane 0 posts the slot's byte count and each
+                // lane issues one page box (page lane / kPanels, panel
+                // lane % kPanels), so one instruction issues a whole tile.  A
+                // page past the sequence, or a bad table entry, is loaded from
+                // just past the pool: TMA fills zeros there (and still counts
+                // the bytes).
+                constexpr int kPagesPerBlock = kBlockN / kPageSize;
+                const int pg = lane / kPanels;  // this lane's page of a block
+                const int pn = lane % kPanels;  // and panel
+                const bool boxes = lane < kPagesPerBlock * kPanels;
+                const int* bt = p.block_table + static_cast<size_t>(seq) * p.max_pages;
+                // Table entries are fetched one block ahead of their use: the
+                // entries of blocks j and j + 1 are in flight at once, kept by
+                // block parity.
+                auto fetch = [&](int blk) {
+                    return (boxes && blk < nmax && blk * kBlockN + pg * kPageSize < Lk)
+                               ? __ldg(bt + blk * kPagesPerBlock + pg)
+                               : -1;
+                };
+                int ent0 = fetch(0), ent1 = fetch(1);
                 bool ok = true;
                 auto load = [&](int i, bool is_k, int j) {
                     const int s = i % kSlots;
 #pragma unroll
                     for (int t = 0; t < kTiles; ++t) {
                         const uint32_t bit = 1u << (t * kMaxSlots + s);
-                        if (ok && (used & bit))  // wait until tile t released the previous occupant
-                            ok = mbar_wait(bar(B_KV_EMPTY + t * kMaxSlots + s), ((par & bit) ? 0u : 1u), abort_flag,
+                        if (ok && (used & bit))
+                            ok = warp_wait(bar(B_KV_EMPTY + t * kMaxSlots + s), ((par & bit) ? 0u : 1u), abort_flag,
                                            p.err, lim);
                     }
                     if (!ok) return;
-                    mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kTile);
-                    const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
-                    const uint32_t dst = sbase + L::kKV + s * L::kTile;
-                    if (p.block_table == nullptr) {
-#pragma unroll
-                        for (int pn = 0; pn < kPanels; ++pn)
-                            tma_load_3d(dst + pn * kPanelBytes, map, bar(B_KV_FULL + s), pn * 64, hk, k_start + j * kBlockN);
-                    } else {
-                        // One box per page.  A page past the sequence, or a bad
-                        // table entry, is loaded from just past the pool: TMA
-                        // fills zeros there (and still counts the bytes).
-                        const int* bt = p.block_table + static_cast<size_t>(seq) * p.max_pages;
-#pragma unroll 1
-                        for (int pg = 0; pg < kBlockN / kPageSize; ++pg) {
-                            const int tok0 = j * kBlockN + pg * kPageSize;
-                            int row = p.num_pages * kPageSize;
-                            if (tok0 < Lk) {
-                                const int page = bt[tok0 / kPageSize];
-                                if (page >= 0 && page < p.num_pages)
-                                    row = page * kPageSize;
-                                else
-                                    atomicOr(p.err, FA_DEVERR_INDEX);
-                            }
-#pragma unroll
-                            for (int pn = 0; pn < kPanels; ++pn)
-                                tma_load_3d(dst + pn * kPanelBytes + pg * kPageSize * 128, map, bar(B_KV_FULL + s), pn * 64,
-                                            hk, row);
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kTile);
+                    __syncwarp();
+                    if (boxes) {
+                        const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+                        const int page = (j & 1) ? ent1 : ent0;
+                        int row = p.num_pages * kPageSize;
+                        if (j * kBlockN + pg * kPageSize < Lk) {
+                            if (page >= 0 && page < p.num_pages)
+                                row = page * kPageSize;
+                            else if (pn == 0 && is_k)
+                                atomicOr(p.err, FA_DEVERR_INDEX);
                         }
+                        tma_load_3d(sbase + L::kKV + s * L::kTile + pn * kPanelBytes + pg * kPageSize * 128, map,
+                                    bar(B_KV_FULL + s), pn * 64, hk, row);
                     }
-                    last_fill[s] = i / kSlots;
-#pragma unroll
-                    for (int t = 0; t < kTiles; ++t) {
-                        const uint32_t bit = 1u << (t * kMaxSlots + s);
-                        if (j < nb[t]) {
-                            used |= bit;
-                            par ^= bit;
-                        } else {
-                            used &= ~bit;
-                        }
-                    }
+                    __syncwarp();
+                    account(i, j);
                 };
                 load(pos_k(0), true, 0);
                 for (int j = 0; ok && j < nmax; ++j) {
                     if (j + 1 < nmax) load(pos_k(j + 1), true, j + 1);
                     load(pos_v(j, nmax), false, j);
+                    // block j is done: its parity slot takes block j + 2
+                    if (j & 1)
+                        ent1 = fetch(j + 2);
+                    else
+                        ent0 = fetch(j + 2);
                 }
-                // Drain: every copy this CTA issued lands before the CTA exits.
+            }
+            // Drain: every copy this CTA issued lands before the CTA exits.
+            if (lane == 0) {
 #pragma unroll
                 for (int s = 0; s < kMaxSlots; ++s)
                     if (s < kSlots && last_fill[s] >= 0) mbar_wait_drain(bar(B_KV_FULL + s), last_fill[s] & 1, lim);
@@ -340,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (nb[t] > 0) mbar_wait_drain(bar(B_Q_FULL + t), 0, lim);
             }
             __syncwarp();
-            if (v_tail) {
+            if (PAGED && v_tail) {
                 // The whole warp zeroes rows [Lk, roundup(Lk, page)) of the
                 // last V tile once it has landed, then releases the last P.V.
                 const int i_last = pos_v(nmax - 1, nmax);
@@ -422,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ok = ok && warp_wait(bar(B_P_FULL + t), j & 1, abort_flag, p.err, lim);
                     wait_item(pos_v(j, nmax));
-                    if (v_tail && j == nmax - 1) ok = ok && warp_wait(bar(B_V_TAIL), 0, abort_flag, p.err, lim);
+                    if (PAGED && v_tail && j == nmax - 1)
+                        ok = ok && warp_wait(bar(B_V_TAIL), 0, abort_flag, p.err, lim);
                     if (!ok) break;
                     issue_pv(j);
                 }
@@ -614,13 +662,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync(kThreads);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PAGED>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      cudaStream_t stream) {
     using L = PrefillSmem<D>;
     static_assert(L::kDyn <= 232448u, "shared memory budget");
     static_assert(L::kSlots <= kMaxSlots, "K/V ring");
-    auto kern = prefill_kernel<D, CAUSAL>;
+    auto kern = prefill_kernel<D, CAUSAL, PAGED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
     if (e != cudaSuccess) return e;
     const int nblk = (p.num_q_blocks + 1) / 2;
@@ -629,12 +677,20 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     return cudaGetLastError();
 }
 
+template <int D, bool PAGED>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                     bool causal, cudaStream_t stream) {
+    return causal ? launch_t<D, true, PAGED>(tq, tk, tv, p, stream) : launch_t<D, false, PAGED>(tq, tk, tv, p, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int d, bool causal, cudaStream_t stream) {
-    if (d == 128) return causal ? launch_t<128, true>(tq, tk, tv, p, stream) : launch_t<128, false>(tq, tk, tv, p, stream);
-    return causal ? launch_t<64, true>(tq, tk, tv, p, stream) : launch_t<64, false>(tq, tk, tv, p, stream);
+    const bool paged = p.block_table != nullptr;
+    if (d == 128)
+        return paged ? launch_d<128, true>(tq, tk, tv, p, causal, stream) : launch_d<128, false>(tq, tk, tv, p, causal, stream);
+    return paged ? launch_d<64, true>(tq, tk, tv, p, causal, stream) : launch_d<64, false>(tq, tk, tv, p, causal, stream);
 }
 
 }  // namespace fa

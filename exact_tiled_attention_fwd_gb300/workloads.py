@@ -55,6 +55,9 @@ CONFIGS = {
 }
 VARLEN_C4 = dict(num_seqs=16, lo=128, hi=4096, H=32, d=64, causal=True)
 PAGED_C5 = dict(B=64, H=32, d=128, lo=512, hi=16384, page_size=PAGE_SIZE)
+# Prefix-cache continuation chunk: cached context plus a chunk of new tokens
+# per sequence, attended through the page table (store_kvcache first).
+CHUNK = dict(num_seqs=16, ctx_lo=512, ctx_hi=8192, new_lo=256, new_hi=2048, H=32, d=128, causal=True)
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -206,3 +209,11 @@ def chunk_inputs(lengths_q, lengths_k, H, d, seed: int, device="cpu", Hkv=None, 
     q = randn_bf16((int(cq[-1]), H, d), seed * 11 + 0, device)
     return ChunkBatch(q, kc, vc, bt.to(device), cq.to(device), ck.to(device), list(lengths_q), list(lengths_k),
                       max(lengths_q), max(lengths_k), num_pages)
+
+
+def chunk_lengths(seed: int = 1240):
+    """(new-token lengths, key lengths) of the continuation workload: key
+    length = cached context U[ctx_lo, ctx_hi] + new tokens U[new_lo, new_hi]."""
+    ctx = uniform_lengths(CHUNK["num_seqs"], CHUNK["ctx_lo"], CHUNK["ctx_hi"], seed)
+    new = uniform_lengths(CHUNK["num_seqs"], CHUNK["new_lo"], CHUNK["new_hi"], seed + 1)
+    return new, [c + n for c, n in zip(ctx, new)]
