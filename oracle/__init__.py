@@ -12,6 +12,10 @@ from .attention import (  # noqa: F401
     attention_varlen,
     attention_paged,
     attention_varlen_paged,
+    attention_qkvpacked,
+    attention_kvpacked,
+    attention_varlen_qkvpacked,
+    attention_varlen_kvpacked,
     store_kvcache,
     gather_paged_kv,
     visible_mask,

@@ -39,6 +39,10 @@ attention_dense          [B, N, H, d] batched multi-head wrapper
 attention_varlen         packed [total, H, d] + cu_seqlens wrapper
 attention_paged          single-query decode over a paged KV pool
 store_kvcache            scatter of one step's K/V rows into the page pool
+attention_qkvpacked      the packed layouts of the page's function table:
+attention_kvpacked         QKV as [.., 3, H, d] or KV as [.., 2, Hkv, d],
+attention_varlen_qkvpacked fixed-length or varlen; each slices the packed
+attention_varlen_kvpacked  tensor and calls the routine above
 attention_varlen_paged   packed prefill whose K/V are read through the page
                          table (a chunk that continues a cached prefix)
 gather_paged_kv          host walk of block_table (the bit-exact gather
@@ -359,3 +363,32 @@ def attention_varlen_paged(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, bloc
             O[qs:qe, h] = o
             lse[h, qs:qe] = l
     return O, lse
+
+
+def attention_qkvpacked(qkv, scale: float, causal: bool):
+    """Packed QKV, fixed length (flash_attn_qkvpacked_func in the dlog.com.cn
+    page's function table, §3.2): qkv is [B, S, 3, H, d], index 0 of the
+    packed axis is Q, 1 is K, 2 is V.  Slices and runs attention_dense."""
+    qkv = np.asarray(qkv)
+    return attention_dense(qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2], scale, causal)
+
+
+def attention_kvpacked(q, kv, scale: float, causal: bool):
+    """Packed KV with a separate Q (flash_attn_kvpacked_func, same table):
+    q [B, S, H, d], kv [B, S, 2, Hkv, d] with K at index 0, V at index 1."""
+    kv = np.asarray(kv)
+    return attention_dense(q, kv[:, :, 0], kv[:, :, 1], scale, causal)
+
+
+def attention_varlen_qkvpacked(qkv, cu_seqlens, scale: float, causal: bool):
+    """Packed QKV, variable length (flash_attn_varlen_qkvpacked_func, §3.3):
+    qkv is [total, 3, H, d]; queries and keys share cu_seqlens."""
+    qkv = np.asarray(qkv)
+    return attention_varlen(qkv[:, 0], qkv[:, 1], qkv[:, 2], cu_seqlens, cu_seqlens, scale, causal)
+
+
+def attention_varlen_kvpacked(q, kv, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool):
+    """Packed KV, variable length (flash_attn_varlen_kvpacked_func, §3.3):
+    q [total_q, H, d], kv [total_k, 2, Hkv, d]."""
+    kv = np.asarray(kv)
+    return attention_varlen(q, kv[:, 0], kv[:, 1], cu_seqlens_q, cu_seqlens_k, scale, causal)
