@@ -51,7 +51,8 @@ WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), packe
             "[512,16384], 16-token pages in a seeded random permutation (fa_paged_fwd); then a prefix-cache "
             "continuation chunk, 16 sequences with cached context U[512,8192] + new tokens U[256,2048], H32 d128 "
             "causal: store the new K/V (fa_store_kvcache), attend through the page table (fa_varlen_paged_fwd), "
-            "and the same shapes with contiguous K/V (fa_varlen_fwd) for comparison")
+            "and the same shapes with contiguous K/V (fa_varlen_fwd) for comparison; then the dense N8192 non-causal "
+            "prefill from one packed [B,N,3,H,d] QKV tensor (fa_qkvpacked_fwd)")
 # DRAM bytes (read + write) per launch from ncu captures of the current
 # kernels (profiles/prefill_kernel_B1H32N8192d128.md: mean of the non-causal
 # and causal launches; profiles/decode_split_kernel_B16H32d128.md: the
@@ -261,6 +262,7 @@ def ours(args, world, rank, local):
     do_varlen = args.case in ("all", "varlen")
     do_decode = args.case in ("all", "decode")
     do_chunk = args.case in ("all", "chunk")
+    do_packed = args.case in ("all", "packed")
     q, k, v = W.dense_inputs(B, N, H, d, SEED_C3, dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -323,6 +325,17 @@ def ours(args, world, rank, local):
         if st != F.FA_OK:
             raise F.FAError(st, "fa_paged_fwd")
 
+    qkv = torch.stack([q, k, v], dim=2).contiguous() if do_packed else q
+    o_p = torch.empty_like(o)
+    lse_p = torch.empty_like(lse)
+
+    def packed():
+        if not do_packed:
+            return
+        st = F.fa_qkvpacked_fwd(qkv, o_p, lse_p, B, H, N, d, scale, False, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_qkvpacked_fwd")
+
     def store():
         if not do_chunk:
             return
@@ -356,13 +369,14 @@ def ours(args, world, rank, local):
         store()
         chunk()
         chunk_contiguous()
+        packed()
     torch.cuda.synchronize()
     st = F.fa_device_status(sp)
     if st != F.FA_OK:
         raise F.FAError(st, "warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(K)]
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -387,6 +401,8 @@ def ours(args, world, rank, local):
         e[6].record(stream)
         chunk_contiguous()
         e[7].record(stream)
+        packed()
+        e[8].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
@@ -402,8 +418,9 @@ def ours(args, world, rank, local):
     t_store = sum(e[4].elapsed_time(e[5]) for e in ev) / K
     t_chunk = sum(e[5].elapsed_time(e[6]) for e in ev) / K
     t_chunk_c = sum(e[6].elapsed_time(e[7]) for e in ev) / K
-    t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c = (
-        max_over_ranks(world, x) for x in (t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c))
+    t_packed = sum(e[7].elapsed_time(e[8]) for e in ev) / K
+    t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed = (
+        max_over_ranks(world, x) for x in (t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed))
     # continuation FLOPs, causal bottom-right, halved-square convention of
     # the varlen leg: 4 d H (Lq (Lk - Lq) + Lq^2 / 2) per sequence
     f_chunk = sum(4.0 * cd * cH * (lq_ * (lk_ - lq_) + lq_ * lq_ / 2) for lq_, lk_ in zip(cl_q, cl_k))
@@ -426,7 +443,8 @@ def ours(args, world, rank, local):
                               "chunk_ms": [t_store, t_chunk, t_chunk_c],
                               "chunk_tflops": f_chunk / (t_chunk * 1e-3) / 1e12 if do_chunk else None,
                               "chunk_contiguous_tflops": f_chunk / (t_chunk_c * 1e-3) / 1e12 if do_chunk else None,
-                              "store_gbs": store_bytes / (t_store * 1e-3) / 1e9 if do_chunk else None}), flush=True)
+                              "store_gbs": store_bytes / (t_store * 1e-3) / 1e9 if do_chunk else None,
+                              "qkvpacked_ms": t_packed}), flush=True)
         return
 
     # ---- end to end through the public API with pinned host buffers
@@ -476,7 +494,7 @@ def ours(args, world, rank, local):
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": t_nc + t_c + t_var + t_dec + t_store + t_chunk + t_chunk_c,
+        "ms_per_step": t_nc + t_c + t_var + t_dec + t_store + t_chunk + t_chunk_c + t_packed,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -498,6 +516,8 @@ def ours(args, world, rank, local):
                                     "frac_bf16_peak": f_chunk / (t_chunk * 1e-3) / 1e12 / peak_tf,
                                     "new_tokens": c_tq, "cached_plus_new_tokens": int(sum(cl_k))},
             "same_chunk_contiguous_kv": {"ms": t_chunk_c, "tflops": f_chunk / (t_chunk_c * 1e-3) / 1e12},
+            "qkvpacked_noncausal": {"ms": t_packed, "tflops": f_nc / (t_packed * 1e-3) / 1e12,
+                                    "frac_bf16_peak": f_nc / (t_packed * 1e-3) / 1e12 / peak_tf},
         },
         "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": tflops / peak_tf, "traffic": PREFILL_TRAFFIC_BYTES,
@@ -507,7 +527,7 @@ def ours(args, world, rank, local):
                             "traffic": DECODE_TRAFFIC_BYTES, "peak_source": f"{peak_src} HBM copy"},
         "e2e": {"value": e2e_tflops * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "prefill legs with q,k,v copied from pinned host memory and O, LSE copied back each step"},
-        "gpu_launches": 8 * K,
+        "gpu_launches": 9 * K,
         "clocks": clk,
         "wall_s_timed": wall,
     }
@@ -524,7 +544,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode", "chunk"], default="all",
+    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode", "chunk", "packed"], default="all",
                     help="run only one leg (for profiling); prints a short line instead of the bench line")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences of the decode leg (profiling)")
     args = ap.parse_args()

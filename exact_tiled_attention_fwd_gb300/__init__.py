@@ -30,7 +30,8 @@ FA_ERR_SCRATCH_CAPACITY = 6
 EXPORTS = (
     "fa_abi_version", "fa_status_string", "fa_fwd", "fa_varlen_fwd", "fa_paged_workspace_size",
     "fa_paged_fwd", "fa_paged_fwd_noalloc", "fa_paged_gather", "fa_device_status", "fa_selftest_wait_timeout",
-    "fa_varlen_paged_fwd", "fa_store_kvcache",
+    "fa_varlen_paged_fwd", "fa_store_kvcache", "fa_qkvpacked_fwd", "fa_kvpacked_fwd", "fa_varlen_qkvpacked_fwd",
+    "fa_varlen_kvpacked_fwd",
 )
 
 _lib = None
@@ -66,6 +67,14 @@ def load(path: str | None = None):
     lib.fa_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_paged_fwd_noalloc.restype = i
     lib.fa_paged_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+    lib.fa_qkvpacked_fwd.restype = i
+    lib.fa_qkvpacked_fwd.argtypes = [vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_kvpacked_fwd.restype = i
+    lib.fa_kvpacked_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_varlen_qkvpacked_fwd.restype = i
+    lib.fa_varlen_qkvpacked_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_varlen_kvpacked_fwd.restype = i
+    lib.fa_varlen_kvpacked_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
     lib.fa_varlen_paged_fwd.restype = i
     lib.fa_varlen_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, i, f, i, vp]
     lib.fa_store_kvcache.restype = i
@@ -120,6 +129,29 @@ def fa_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, max_seq
     return load().fa_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
                                 _ptr(cu_seqlens_k), num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k,
                                 H, Hkv, d, scale, int(bool(causal)), _stream(stream))
+
+
+def fa_qkvpacked_fwd(qkv, o, lse, B, H, N, d, scale, causal, stream=None) -> int:
+    return load().fa_qkvpacked_fwd(_ptr(qkv), _ptr(o), _ptr(lse), B, H, N, d, scale, int(bool(causal)),
+                                   _stream(stream))
+
+
+def fa_kvpacked_fwd(q, kv, o, lse, B, H, Hkv, N, d, scale, causal, stream=None) -> int:
+    return load().fa_kvpacked_fwd(_ptr(q), _ptr(kv), _ptr(o), _ptr(lse), B, H, Hkv, N, d, scale, int(bool(causal)),
+                                  _stream(stream))
+
+
+def fa_varlen_qkvpacked_fwd(qkv, o, lse, cu_seqlens, num_seqs, max_seqlen, total, H, d, scale, causal,
+                            stream=None) -> int:
+    return load().fa_varlen_qkvpacked_fwd(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(cu_seqlens), num_seqs, max_seqlen,
+                                          total, H, d, scale, int(bool(causal)), _stream(stream))
+
+
+def fa_varlen_kvpacked_fwd(q, kv, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, max_seqlen_q, max_seqlen_k,
+                           total_q, total_k, H, Hkv, d, scale, causal, stream=None) -> int:
+    return load().fa_varlen_kvpacked_fwd(_ptr(q), _ptr(kv), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                                         _ptr(cu_seqlens_k), num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k,
+                                         H, Hkv, d, scale, int(bool(causal)), _stream(stream))
 
 
 def fa_varlen_paged_fwd(q, k_cache, v_cache, o, lse, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
@@ -288,4 +320,37 @@ def attention_varlen_paged(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, bloc
                              cu_seqlens_q.numel() - 1, max_seqlen_q, max_seqlen_k, total_q, H, Hkv, d, page_size,
                              num_pages, block_table.shape[1], scale, causal, stream)
     _check(st, "fa_varlen_paged_fwd")
+    return out, lse
+
+
+def attention_qkvpacked(qkv, scale=None, causal=False, out=None, lse=None, stream=None):
+    """Packed QKV forward.  qkv: [B, N, 3, H, d] bf16.  Returns (O [B, N, H, d],
+    LSE [B, H, N])."""
+    import torch
+
+    _req(qkv, "qkv", torch.bfloat16)
+    B, N, three, H, d = qkv.shape
+    if three != 3:
+        raise ValueError("qkv must be [B, N, 3, H, d]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty((B, N, H, d), dtype=qkv.dtype, device=qkv.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=qkv.device) if lse is None else lse
+    _check(fa_qkvpacked_fwd(qkv, out, lse, B, H, N, d, scale, causal, stream), "fa_qkvpacked_fwd")
+    return out, lse
+
+
+def attention_kvpacked(q, kv, scale=None, causal=False, out=None, lse=None, stream=None):
+    """Packed KV forward.  q: [B, N, H, d], kv: [B, N, 2, Hkv, d] bf16."""
+    import torch
+
+    _req(q, "q", torch.bfloat16)
+    _req(kv, "kv", torch.bfloat16)
+    B, N, H, d = q.shape
+    Hkv = kv.shape[3]
+    if kv.shape != (B, N, 2, Hkv, d):
+        raise ValueError("kv must be [B, N, 2, Hkv, d] matching q")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(fa_kvpacked_fwd(q, kv, out, lse, B, H, Hkv, N, d, scale, causal, stream), "fa_kvpacked_fwd")
     return out, lse

@@ -17,7 +17,7 @@ __device__ unsigned int g_fa_error_word;
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 constexpr int kMaxDevices = 64;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -70,10 +70,13 @@ fa_status ensure_init(unsigned int** err_out) {
 // 3-D view (d, heads, rows) of a [rows, heads, d] bf16 tensor; a box is 64
 // elements of d (128 bytes, the swizzle span) x 1 head x box_rows rows (a
 // 128-row tile, or one 16-token page of the paged pool).
+// row_stride is in elements between consecutive rows (heads * d for a dense
+// tensor, more for one slot of a packed [rows, 3 or 2, heads, d] tensor).
 fa_status make_map(CUtensorMap* map, const void* base, int d, int heads, long long rows,
-                   int box_rows = fa::kBlockM) {
+                   int box_rows = fa::kBlockM, long long row_stride = 0) {
+    if (row_stride == 0) row_stride = static_cast<long long>(heads) * d;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(row_stride) * 2};
     cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -110,10 +113,22 @@ const char* fa_status_string(int status) {
     }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N, int d,
-           float scale, int causal, void* stream) {
-    if (!q || !k || !v || !o) return FA_ERR_INVALID;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID;
+}  // extern "C"
+
+namespace {
+
+// One operand of the prefill: its first element and the elements between
+// consecutive rows (tokens).
+struct Operand {
+    const void* base;
+    long long row_stride;
+};
+
+fa_status dense_impl(Operand q, Operand k, Operand v, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+                     float scale, int causal, void* stream) {
+    if (!q.base || !k.base || !v.base || !o) return FA_ERR_INVALID;
+    if (!aligned16(q.base) || !aligned16(k.base) || !aligned16(v.base) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID;
     if (B < 1 || H < 1 || Hkv < 1 || N < 1 || H % Hkv != 0 || !scale_ok(scale)) return FA_ERR_INVALID;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     const long long rows = static_cast<long long>(B) * N;
@@ -122,9 +137,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     fa_status st = ensure_init(&err);
     if (st != FA_OK) return st;
     CUtensorMap tq, tk, tv;
-    if ((st = make_map(&tq, q, d, H, rows)) != FA_OK) return st;
-    if ((st = make_map(&tk, k, d, Hkv, rows)) != FA_OK) return st;
-    if ((st = make_map(&tv, v, d, Hkv, rows)) != FA_OK) return st;
+    if ((st = make_map(&tq, q.base, d, H, rows, fa::kBlockM, q.row_stride)) != FA_OK) return st;
+    if ((st = make_map(&tk, k.base, d, Hkv, rows, fa::kBlockM, k.row_stride)) != FA_OK) return st;
+    if ((st = make_map(&tv, v.base, d, Hkv, rows, fa::kBlockM, v.row_stride)) != FA_OK) return st;
     fa::PrefillParams p{};
     p.o = o;
     p.lse = lse;
@@ -148,11 +163,12 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
 }
 
-int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
-                  const int* cu_seqlens_k, int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q,
-                  int total_k, int H, int Hkv, int d, float scale, int causal, void* stream) {
-    if (!q || !k || !v || !o || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_INVALID;
+fa_status varlen_impl(Operand q, Operand k, Operand v, void* o, float* lse, const int* cu_seqlens_q,
+                      const int* cu_seqlens_k, int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q,
+                      int total_k, int H, int Hkv, int d, float scale, int causal, void* stream) {
+    if (!q.base || !k.base || !v.base || !o || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID;
+    if (!aligned16(q.base) || !aligned16(k.base) || !aligned16(v.base) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
         return FA_ERR_INVALID;
     if (num_seqs < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 ||
@@ -164,9 +180,9 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
     fa_status st = ensure_init(&err);
     if (st != FA_OK) return st;
     CUtensorMap tq, tk, tv;
-    if ((st = make_map(&tq, q, d, H, total_q)) != FA_OK) return st;
-    if ((st = make_map(&tk, k, d, Hkv, total_k)) != FA_OK) return st;
-    if ((st = make_map(&tv, v, d, Hkv, total_k)) != FA_OK) return st;
+    if ((st = make_map(&tq, q.base, d, H, total_q, fa::kBlockM, q.row_stride)) != FA_OK) return st;
+    if ((st = make_map(&tk, k.base, d, Hkv, total_k, fa::kBlockM, k.row_stride)) != FA_OK) return st;
+    if ((st = make_map(&tv, v.base, d, Hkv, total_k, fa::kBlockM, v.row_stride)) != FA_OK) return st;
     fa::PrefillParams p{};
     p.o = o;
     p.lse = lse;
@@ -188,6 +204,60 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
     p.wait_limit_ns = wait_limit_ns();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
+}
+
+// Slot `slot` of a packed [rows, n, heads, d] bf16 tensor.
+Operand packed(const void* base, int slot, int n, int heads, int d) {
+    if (base == nullptr || heads < 1 || d < 1) return Operand{base, 0};  // sizes are rejected by the caller
+    return Operand{static_cast<const uint16_t*>(base) + static_cast<size_t>(slot) * heads * d,
+                   static_cast<long long>(n) * heads * d};
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+           float scale, int causal, void* stream) {
+    return dense_impl(Operand{q, 0}, Operand{k, 0}, Operand{v, 0}, o, lse, B, H, Hkv, N, d, scale, causal, stream);
+}
+
+int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q,
+                  int total_k, int H, int Hkv, int d, float scale, int causal, void* stream) {
+    return varlen_impl(Operand{q, 0}, Operand{k, 0}, Operand{v, 0}, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs,
+                       max_seqlen_q, max_seqlen_k, total_q, total_k, H, Hkv, d, scale, causal, stream);
+}
+
+int fa_qkvpacked_fwd(const void* qkv, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+                     void* stream) {
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return dense_impl(packed(qkv, 0, 3, H, d), packed(qkv, 1, 3, H, d), packed(qkv, 2, 3, H, d), o, lse, B, H, H, N,
+                      d, scale, causal, stream);
+}
+
+int fa_kvpacked_fwd(const void* q, const void* kv, void* o, float* lse, int B, int H, int Hkv, int N, int d,
+                    float scale, int causal, void* stream) {
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return dense_impl(Operand{q, 0}, packed(kv, 0, 2, Hkv, d), packed(kv, 1, 2, Hkv, d), o, lse, B, H, Hkv, N, d,
+                      scale, causal, stream);
+}
+
+int fa_varlen_qkvpacked_fwd(const void* qkv, void* o, float* lse, const int* cu_seqlens, int num_seqs,
+                            int max_seqlen, int total, int H, int d, float scale, int causal, void* stream) {
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return varlen_impl(packed(qkv, 0, 3, H, d), packed(qkv, 1, 3, H, d), packed(qkv, 2, 3, H, d), o, lse,
+                       cu_seqlens, cu_seqlens, num_seqs, max_seqlen, max_seqlen, total, total, H, H, d, scale, causal,
+                       stream);
+}
+
+int fa_varlen_kvpacked_fwd(const void* q, const void* kv, void* o, float* lse, const int* cu_seqlens_q,
+                           const int* cu_seqlens_k, int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q,
+                           int total_k, int H, int Hkv, int d, float scale, int causal, void* stream) {
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return varlen_impl(Operand{q, 0}, packed(kv, 0, 2, Hkv, d), packed(kv, 1, 2, Hkv, d), o, lse, cu_seqlens_q,
+                       cu_seqlens_k, num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, H, Hkv, d, scale,
+                       causal, stream);
 }
 
 int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,

@@ -104,6 +104,33 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
                   int H, int Hkv, int d, float scale, int causal, void* stream);
 
 /*
+ * Packed layouts (the qkvpacked / kvpacked rows of the dlog.com.cn page's
+ * function table, §3.2 and §3.3): the result a single projection produces,
+ * passed without splitting it.  O and LSE are laid out as in fa_fwd /
+ * fa_varlen_fwd.
+ *   fa_qkvpacked_fwd        qkv : [B, N, 3, H, d] bf16 (index 0 Q, 1 K, 2 V;
+ *                                 H query and key/value heads)
+ *   fa_kvpacked_fwd         q   : [B, N, H, d];  kv : [B, N, 2, Hkv, d]
+ *                                 (index 0 K, 1 V)
+ *   fa_varlen_qkvpacked_fwd qkv : [total, 3, H, d]; one cu_seqlens for Q and K
+ *   fa_varlen_kvpacked_fwd  q   : [total_q, H, d]; kv : [total_k, 2, Hkv, d]
+ * Same arguments, conventions and errors as fa_fwd / fa_varlen_fwd
+ * otherwise.  The packed tensors are read in place, through strided tensor
+ * maps: nothing is copied.
+ */
+int fa_qkvpacked_fwd(const void* qkv, void* o, float* lse, int B, int H, int N, int d,
+                     float scale, int causal, void* stream);
+int fa_kvpacked_fwd(const void* q, const void* kv, void* o, float* lse,
+                    int B, int H, int Hkv, int N, int d, float scale, int causal, void* stream);
+int fa_varlen_qkvpacked_fwd(const void* qkv, void* o, float* lse, const int* cu_seqlens,
+                            int num_seqs, int max_seqlen, int total, int H, int d,
+                            float scale, int causal, void* stream);
+int fa_varlen_kvpacked_fwd(const void* q, const void* kv, void* o, float* lse,
+                           const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                           int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                           int H, int Hkv, int d, float scale, int causal, void* stream);
+
+/*
  * Packed variable-length prefill whose keys and values are read through a
  * page table (the prefill entry point with block_table of the dlog.com.cn
  * page, "v3 实际调用的两个函数": a chunk that continues a cached prefix reads

@@ -51,7 +51,7 @@ def test_status_strings(lib):
     for code in range(6):
         assert lib.status_string(code).startswith("FA_")
     assert "unknown" in lib.status_string(99)
-    assert lib.fa_abi_version() == 2
+    assert lib.fa_abi_version() == 3
 
 
 def test_validation_without_gpu(lib):
@@ -92,6 +92,14 @@ def test_validation_without_gpu(lib):
     assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 128, 16, 30, 12, 0.1, 1, S) == lib.FA_ERR_INVALID
     assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 3, 128, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_INVALID
     assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 96, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_UNSUPPORTED
+    # packed layouts: null tensors, d, GQA with packed QKV is not expressible
+    assert lib.fa_qkvpacked_fwd(0, A, None, 1, 4, 8, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_qkvpacked_fwd(A, A, None, 1, 4, 8, 96, 0.1, 0, S) == lib.FA_ERR_UNSUPPORTED
+    assert lib.fa_qkvpacked_fwd(A + 8, A, None, 1, 4, 8, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_kvpacked_fwd(A, 0, A, None, 1, 4, 2, 8, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_kvpacked_fwd(A, A, A, None, 1, 4, 3, 8, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_varlen_qkvpacked_fwd(A, A, None, 0, 1, 8, 8, 4, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
+    assert lib.fa_varlen_kvpacked_fwd(A, A, A, None, A, A, 1, 8, 8, 8, 8, 4, 2, 64, 0.0, 0, S) == lib.FA_ERR_INVALID
     # store_kvcache: null slot map, unaligned cache, negative token count, d
     sk = lib.fa_store_kvcache
     assert sk(A, A, A, A, 0, 8, 2, 128, 16, 4, S) == lib.FA_ERR_INVALID
