@@ -90,7 +90,11 @@ __device__ __forceinline__ void axpy8(float (&o)[8], float p, const uint4& v) {
     o[7] = fmaf(p, bf16hi_to_f32(v.w), o[7]);
 }
 
-template <int D>
+// One warp per (sequence, split, G query heads of one kv head).  With
+// grouped-query attention the G heads share every K/V row the warp loads, so
+// each row is read once per group instead of once per query head; G = 1 is
+// plain multi-head attention.
+template <int D, int G>
 __global__ void __launch_bounds__(kDecodeWarps * 32) decode_split_kernel(const DecodeParams p) {
     constexpr int LPR = D / 8;         // lanes per key row
     constexpr int RPI = 32 / LPR;      // rows per warp load
@@ -98,37 +102,42 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_split_kernel(const D
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.z;
-    const int h = blockIdx.y * kDecodeWarps + warp;
+    const int h0 = (blockIdx.y * kDecodeWarps + warp) * G;  // first of this warp's heads
     const int split = blockIdx.x;
-    if (h >= p.H) return;
+    if (h0 >= p.H) return;
     const int L = clamp_seqlen(__ldg(p.seqlens + b), p.max_seqlen, p.err, split == 0 && lane == 0);
     const int t0 = split * p.split_tokens;
     if (t0 >= L) return;
     const int t1 = min(L, t0 + p.split_tokens);
-    const int hk = h / p.group;
+    const int hk = h0 / p.group;  // G divides the group, so all G heads share it
     const int g = lane / LPR;  // row group within a warp load
     const int c = lane % LPR;  // 8-element chunk of the row
 
-    // q chunk, pre-multiplied by scale * log2(e) so scores are in log2 units
-    float qf[8];
-    {
+    // q chunks, pre-multiplied by scale * log2(e) so scores are in log2 units
+    float qf[G][8];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
         const uint4 qv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                         (static_cast<size_t>(b) * p.H + h) * D + c * 8);
-        qf[0] = bf16lo_to_f32(qv.x) * p.scale_log2;
-        qf[1] = bf16hi_to_f32(qv.x) * p.scale_log2;
-        qf[2] = bf16lo_to_f32(qv.y) * p.scale_log2;
-        qf[3] = bf16hi_to_f32(qv.y) * p.scale_log2;
-        qf[4] = bf16lo_to_f32(qv.z) * p.scale_log2;
-        qf[5] = bf16hi_to_f32(qv.z) * p.scale_log2;
-        qf[6] = bf16lo_to_f32(qv.w) * p.scale_log2;
-        qf[7] = bf16hi_to_f32(qv.w) * p.scale_log2;
+                                                         (static_cast<size_t>(b) * p.H + h0 + j) * D + c * 8);
+        qf[j][0] = bf16lo_to_f32(qv.x) * p.scale_log2;
+        qf[j][1] = bf16hi_to_f32(qv.x) * p.scale_log2;
+        qf[j][2] = bf16lo_to_f32(qv.y) * p.scale_log2;
+        qf[j][3] = bf16hi_to_f32(qv.y) * p.scale_log2;
+        qf[j][4] = bf16lo_to_f32(qv.z) * p.scale_log2;
+        qf[j][5] = bf16hi_to_f32(qv.z) * p.scale_log2;
+        qf[j][6] = bf16lo_to_f32(qv.w) * p.scale_log2;
+        qf[j][7] = bf16hi_to_f32(qv.w) * p.scale_log2;
     }
     const uint16_t* kc = static_cast<const uint16_t*>(p.k_cache);
     const uint16_t* vc = static_cast<const uint16_t*>(p.v_cache);
-    float m = neg_inf(), l = 0.f;
-    float acc[8];
+    float m[G], l[G], acc[G][8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int j = 0; j < G; ++j) {
+        m[j] = neg_inf();
+        l[j] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+    }
 
     for (int pg = t0 / kPageSize; pg * kPageSize < t1; ++pg) {
         const int page = lookup_page(p.block_table, p.max_pages, p.num_pages, b, pg, p.err);
@@ -144,51 +153,57 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_split_kernel(const D
             const size_t off = paged_row_offset(page, i * RPI + g, p.Hkv, hk, D) + c * 8;
             vv[i] = ldg_stream(vc + off);
         }
-        float s[NI];
 #pragma unroll
-        for (int i = 0; i < NI; ++i) s[i] = dot8(qf, kv[i]);
+        for (int j = 0; j < G; ++j) {
+            float s[NI];
 #pragma unroll
-        for (int off = LPR / 2; off >= 1; off >>= 1) {
+            for (int i = 0; i < NI; ++i) s[i] = dot8(qf[j], kv[i]);
 #pragma unroll
-            for (int i = 0; i < NI; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
+            for (int off = LPR / 2; off >= 1; off >>= 1) {
+#pragma unroll
+                for (int i = 0; i < NI; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
+            }
+            float mp = neg_inf();
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const int tok = pg * kPageSize + i * RPI + g;
+                if (tok >= t1) s[i] = neg_inf();
+                mp = fmaxf(mp, s[i]);
+            }
+#pragma unroll
+            for (int off = LPR; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, off));
+            const float m_new = fmaxf(m[j], mp);
+            const float mu = m_new == neg_inf() ? 0.f : m_new;
+            const float alpha = ex2(m[j] - mu);  // m = -inf -> 0
+            l[j] *= alpha;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j][e] *= alpha;
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const float pi = ex2(s[i] - mu);
+                l[j] += pi;
+                axpy8(acc[j], pi, vv[i]);
+            }
+            m[j] = m_new;
         }
-        float mp = neg_inf();
-#pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            const int tok = pg * kPageSize + i * RPI + g;
-            if (tok >= t1) s[i] = neg_inf();
-            mp = fmaxf(mp, s[i]);
-        }
-#pragma unroll
-        for (int off = LPR; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, off));
-        const float m_new = fmaxf(m, mp);
-        const float mu = m_new == neg_inf() ? 0.f : m_new;
-        const float alpha = ex2(m - mu);  // m = -inf -> 0
-        l *= alpha;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] *= alpha;
-#pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            const float pi = ex2(s[i] - mu);
-            l += pi;
-            axpy8(acc, pi, vv[i]);
-        }
-        m = m_new;
     }
     // Sum the row groups: every lane of a group holds the same l; chunks add.
 #pragma unroll
-    for (int off = LPR; off < 32; off <<= 1) {
-        l += __shfl_xor_sync(0xffffffffu, l, off);
+    for (int j = 0; j < G; ++j) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+        for (int off = LPR; off < 32; off <<= 1) {
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j][e] += __shfl_xor_sync(0xffffffffu, acc[j][e], off);
+        }
+        const size_t slot = (static_cast<size_t>(b) * p.H + h0 + j) * p.max_splits + split;
+        if (g == 0) {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D + c * 8);
+            dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+            dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+        }
+        if (lane == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(m[j], l[j]);
     }
-    const size_t slot = (static_cast<size_t>(b) * p.H + h) * p.max_splits + split;
-    if (g == 0) {
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D + c * 8);
-        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    }
-    if (lane == 0) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(m, l);
 }
 
 template <int D>
@@ -304,20 +319,36 @@ __global__ void wait_selftest_kernel(unsigned int* err, unsigned long long limit
 
 }  // namespace
 
+namespace {
+
+template <int D, int G>
+cudaError_t launch_split(const DecodeParams& p, cudaStream_t stream) {
+    const int warps = (p.H + G - 1) / G;
+    dim3 grid(p.max_splits, (warps + kDecodeWarps - 1) / kDecodeWarps, p.B);
+    decode_split_kernel<D, G><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Query heads per warp: up to 4 heads of a kv group (the largest count that
+// divides the group).  8 heads at d = 64 fit the registers too, but leave so
+// few warps per SM that the loads stop overlapping (measured slower).
+template <int D>
+cudaError_t launch_split_grouped(const DecodeParams& p, cudaStream_t stream) {
+    if (p.group % 4 == 0) return launch_split<D, 4>(p, stream);
+    if (p.group % 2 == 0) return launch_split<D, 2>(p, stream);
+    return launch_split<D, 1>(p, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream) {
-    dim3 grid(p.max_splits, (p.H + kDecodeWarps - 1) / kDecodeWarps, p.B);
     dim3 cgrid((p.B * p.H + kDecodeWarps - 1) / kDecodeWarps);
-    if (d == 128) {
-        decode_split_kernel<128><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+    cudaError_t e = d == 128 ? launch_split_grouped<128>(p, stream) : launch_split_grouped<64>(p, stream);
+    if (e != cudaSuccess) return e;
+    if (d == 128)
         decode_combine_kernel<128><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
-    } else {
-        decode_split_kernel<64><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+    else
         decode_combine_kernel<64><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
-    }
     return cudaGetLastError();
 }
 

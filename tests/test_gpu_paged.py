@@ -47,8 +47,13 @@ def test_empty_sequence(fa):
     check_full(fa, [0, 5, 0, 40], 2, 128, seed=21)
 
 
-def test_gqa_decode(fa):
-    check_full(fa, [700, 33, 1], 8, 128, seed=22, Hkv=2)
+@pytest.mark.parametrize("H,Hkv,d", [(8, 2, 128), (8, 4, 128), (32, 2, 128), (16, 2, 64), (32, 2, 64),
+                                     (6, 2, 64), (4, 4, 64), (12, 3, 128)])
+def test_gqa_decode(fa, H, Hkv, d):
+    """Query heads grouped over kv heads: the decode warps take 1, 2, 4 or 8
+    heads of one group (groups of 2, 3, 4, 8, 16) and read each K/V row once
+    for all of them."""
+    check_full(fa, [700, 33, 1, 1500], H, d, seed=22 + H + Hkv, Hkv=Hkv)
 
 
 def test_c5_sampled_heads(fa):
