@@ -53,11 +53,11 @@ WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), packe
             "causal: store the new K/V (fa_store_kvcache), attend through the page table (fa_varlen_paged_fwd), "
             "and the same shapes with contiguous K/V (fa_varlen_fwd) for comparison; then the dense N8192 non-causal "
             "prefill from one packed [B,N,3,H,d] QKV tensor (fa_qkvpacked_fwd)")
-# DRAM bytes (read + write) per launch from ncu captures of the current
-# kernels (profiles/prefill_kernel_B1H32N8192d128.md: mean of the non-causal
-# and causal launches; profiles/decode_split_kernel_B16H32d128.md: the
-# 16-sequence capture scaled by cached tokens to the 64-sequence launch).
-# Set to None whenever a kernel changes after its capture.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
+# ncu captures of the current kernels: for prefill the mean of the N=8192
+# non-causal and causal launches; for decode a 16-sequence capture scaled by
+# cached tokens to the 64-sequence launch.  Set to None whenever a kernel
+# changes after its capture.
 PREFILL_TRAFFIC_BYTES = 418.1e6
 DECODE_TRAFFIC_BYTES = 9.29e9
 
@@ -272,7 +272,8 @@ def ours(args, world, rank, local):
     vo = torch.empty_like(vq)
     vlse = torch.empty((vH, vq.shape[0]), dtype=torch.float32, device=dev)
     lens = W.c5_lengths()[: args.decode_batch] if do_decode else [16]
-    pb = W.paged_inputs(lens, C5["H"], C5["d"], SEED_C5, dev, pool_on_device=True)
+    hkv5 = args.decode_hkv
+    pb = W.paged_inputs(lens, C5["H"], C5["d"], SEED_C5, dev, Hkv=hkv5, pool_on_device=True)
     B5, H5, d5 = len(lens), C5["H"], C5["d"]
     o5 = torch.empty_like(pb.q)
     l5 = torch.empty((B5, H5), dtype=torch.float32, device=dev)
@@ -320,7 +321,7 @@ def ours(args, world, rank, local):
     def decode():
         if not do_decode:
             return
-        st = F.fa_paged_fwd(pb.q, pb.k_cache, pb.v_cache, pb.block_table, pb.seqlens, o5, l5, B5, H5, H5, d5, 16,
+        st = F.fa_paged_fwd(pb.q, pb.k_cache, pb.v_cache, pb.block_table, pb.seqlens, o5, l5, B5, H5, hkv5, d5, 16,
                             pb.num_pages, maxp, pb.max_seqlen, 1.0 / math.sqrt(d5), True, ws, ws_bytes, sp)
         if st != F.FA_OK:
             raise F.FAError(st, "fa_paged_fwd")
@@ -442,7 +443,7 @@ def ours(args, world, rank, local):
     f_nc = prefill_flops(N, d, H, B, False)
     f_c = prefill_flops(N, d, H, B, True)
     tflops = job_tflops(1, f_nc + f_c, t_nc + t_c)  # per replica; the job value multiplies by world
-    kv_bytes = float(sum(lens)) * H5 * d5 * 2 * 2
+    kv_bytes = float(sum(lens)) * hkv5 * d5 * 2 * 2
     dec_bytes = kv_bytes + 2 * B5 * H5 * d5 * 2 + B5 * H5 * 4 + sum((L + 15) // 16 for L in lens) * 4
     gbs = dec_bytes / (t_dec * 1e-3) / 1e9
     peak_tf, peak_gbs, peak_src = load_peaks()
@@ -561,6 +562,8 @@ def main():
     ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode", "chunk", "packed"], default="all",
                     help="run only one leg (for profiling); prints a short line instead of the bench line")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences of the decode leg (profiling)")
+    ap.add_argument("--decode-hkv", type=int, default=32,
+                    help="kv heads of the decode leg (32 = plain multi-head; fewer = grouped queries, profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -17,7 +17,7 @@ What it computes (the plain definition, no tiling, no fusion):
 All arithmetic is float64.  Inputs are whatever the caller passes (the tests
 pass the very bf16 values the GPU sees, upcast exactly to float64).
 
-Readings of points the pages leave open (each is listed in the design doc too):
+Readings of points the pages leave open:
 
 * scale is an explicit argument (the pages' 1/sqrt(d) is garbled on two of
   the three pages and omitted in the worked example);
