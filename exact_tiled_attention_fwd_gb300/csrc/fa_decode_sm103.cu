@@ -31,6 +31,11 @@ namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kDecodeWarps = 8;
+// Warps per split CTA: eight heads' warps for plain multi-head decode (one
+// page row of eight heads is contiguous), four for grouped queries, whose
+// larger register count would otherwise leave one CTA, eight warps, per SM.
+template <int G>
+__host__ __device__ constexpr int split_warps() { return G == 1 ? 8 : 4; }
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
@@ -95,14 +100,14 @@ __device__ __forceinline__ void axpy8(float (&o)[8], float p, const uint4& v) {
 // each row is read once per group instead of once per query head; G = 1 is
 // plain multi-head attention.
 template <int D, int G>
-__global__ void __launch_bounds__(kDecodeWarps * 32) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(const DecodeParams p) {
     constexpr int LPR = D / 8;         // lanes per key row
     constexpr int RPI = 32 / LPR;      // rows per warp load
     constexpr int NI = kPageSize / RPI;  // loads per lane per page (K and V each)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.z;
-    const int h0 = (blockIdx.y * kDecodeWarps + warp) * G;  // first of this warp's heads
+    const int h0 = (blockIdx.y * split_warps<G>() + warp) * G;  // first of this warp's heads
     const int split = blockIdx.x;
     if (h0 >= p.H) return;
     const int L = clamp_seqlen(__ldg(p.seqlens + b), p.max_seqlen, p.err, split == 0 && lane == 0);
@@ -324,8 +329,9 @@ namespace {
 template <int D, int G>
 cudaError_t launch_split(const DecodeParams& p, cudaStream_t stream) {
     const int warps = (p.H + G - 1) / G;
-    dim3 grid(p.max_splits, (warps + kDecodeWarps - 1) / kDecodeWarps, p.B);
-    decode_split_kernel<D, G><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
+    constexpr int kW = split_warps<G>();
+    dim3 grid(p.max_splits, (warps + kW - 1) / kW, p.B);
+    decode_split_kernel<D, G><<<grid, kW * 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
