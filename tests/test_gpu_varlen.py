@@ -64,6 +64,13 @@ def test_q_longer_than_k(fa):
     check_full(fa, [300, 20], 2, 64, True, seed=14, lk=[40, 3])
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_length_sequences(fa, causal):
+    """Sequences with no queries are skipped; a sequence whose queries see no
+    key (Lk = 0) gets O = 0 and LSE = -inf."""
+    check_full(fa, [0, 5, 0, 130, 7], 2, 64, causal, seed=17, lk=[3, 0, 0, 200, 7])
+
+
 def test_c4_sampled(fa):
     """16 sequences, lengths U[128, 4096], H32 d64, causal: the full-size
     launch bench-style, sampled rows of every sequence and head."""
