@@ -16,6 +16,8 @@ from .attention import (  # noqa: F401
     attention_kvpacked,
     attention_varlen_qkvpacked,
     attention_varlen_kvpacked,
+    attention_backward_head,
+    attention_backward_dense,
     store_kvcache,
     gather_paged_kv,
     visible_mask,

@@ -43,6 +43,10 @@ attention_qkvpacked      the packed layouts of the page's function table:
 attention_kvpacked         QKV as [.., 3, H, d] or KV as [.., 2, Hkv, d],
 attention_varlen_qkvpacked fixed-length or varlen; each slices the packed
 attention_varlen_kvpacked  tensor and calls the routine above
+attention_backward_head  gradients dQ, dK, dV of one head (the backward pass
+attention_backward_dense   the pages describe: P recomputed from the saved
+                           logsumexp, then the chain rule), and the batched
+                           [B, N, H, d] wrapper
 attention_varlen_paged   packed prefill whose K/V are read through the page
                          table (a chunk that continues a cached prefix)
 gather_paged_kv          host walk of block_table (the bit-exact gather
@@ -392,3 +396,47 @@ def attention_varlen_kvpacked(q, kv, cu_seqlens_q, cu_seqlens_k, scale: float, c
     q [total_q, H, d], kv [total_k, 2, Hkv, d]."""
     kv = np.asarray(kv)
     return attention_varlen(q, kv[:, 0], kv[:, 1], cu_seqlens_q, cu_seqlens_k, scale, causal)
+
+
+def attention_backward_head(q, k, v, do, scale: float, causal: bool = False):
+    """Gradients of O = softmax(scale Q K^T) V for one head, given dO.
+
+    The steps the pages give for the backward pass (the lqnn.cn FlashAttention
+    article §2.3 and §4.3, the yulong.wang page §2.3): recompute S and P (here
+    from the definition; the kernels use the forward's logsumexp), then apply
+    the chain rule, subtracting the row sum in dS:
+      dV = P^T dO
+      dP = dO V^T
+      dS = P * (dP - D),  D_i = sum_j P_ij dP_ij = sum_d dO_id O_id
+           (the row sum subtracted in the softmax backward)
+      dQ = scale dS K,   dK = scale dS^T Q
+    Masked entries have P = 0, hence dS = 0.  A row with no visible key has
+    O = 0 and contributes nothing.  q: [Lq, d], k, v: [Lk, d], do: [Lq, d].
+    Returns (dq, dk, dv) in float64.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    Lq, Lk = q.shape[0], k.shape[0]
+    _, _, _, P = attention_head(q, k, v, scale, causal, return_sp=True)
+    vis = visible_mask(Lq, Lk, causal)
+    P = np.where(vis, P, 0.0)
+    O = P @ v
+    dv = P.T @ do
+    dP = do @ v.T
+    D = np.sum(do * O, axis=1)
+    dS = P * (dP - D[:, None])
+    dq = scale * (dS @ k)
+    dk = scale * (dS.T @ q)
+    return dq, dk, dv
+
+
+def attention_backward_dense(q, k, v, do, scale: float, causal: bool):
+    """Batched backward, layout [B, N, H, d] for q, k, v, do (multi-head,
+    H_kv = H).  Returns dq, dk, dv of the same shapes, float64."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, N, H, d = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            dq[b, :, h], dk[b, :, h], dv[b, :, h] = attention_backward_head(
+                q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h], scale, causal)
+    return dq, dk, dv
