@@ -18,6 +18,7 @@ from .attention import (  # noqa: F401
     attention_varlen_kvpacked,
     attention_backward_head,
     attention_backward_dense,
+    attention_backward_varlen,
     store_kvcache,
     gather_paged_kv,
     visible_mask,

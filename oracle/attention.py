@@ -45,8 +45,9 @@ attention_varlen_qkvpacked fixed-length or varlen; each slices the packed
 attention_varlen_kvpacked  tensor and calls the routine above
 attention_backward_head  gradients dQ, dK, dV of one head (the backward pass
 attention_backward_dense   the pages describe: P recomputed from the saved
-                           logsumexp, then the chain rule), and the batched
-                           [B, N, H, d] wrapper
+attention_backward_varlen  logsumexp, then the chain rule), and the batched
+                           [B, N, H, d] and packed varlen wrappers (grouped
+                           kv heads sum their query heads' dK, dV)
 attention_varlen_paged   packed prefill whose K/V are read through the page
                          table (a chunk that continues a cached prefix)
 gather_paged_kv          host walk of block_table (the bit-exact gather
@@ -430,13 +431,38 @@ def attention_backward_head(q, k, v, do, scale: float, causal: bool = False):
 
 
 def attention_backward_dense(q, k, v, do, scale: float, causal: bool):
-    """Batched backward, layout [B, N, H, d] for q, k, v, do (multi-head,
-    H_kv = H).  Returns dq, dk, dv of the same shapes, float64."""
+    """Batched backward: q, do [B, N, H, d], k, v [B, N, Hkv, d].  Query
+    head h reads kv head h // (H // Hkv), so a kv head's dK and dV are the
+    sums over its query heads.  Returns dq, dk, dv (float64)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, N, H, d = q.shape
+    g = H // k.shape[2]
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     for b in range(B):
         for h in range(H):
-            dq[b, :, h], dk[b, :, h], dv[b, :, h] = attention_backward_head(
-                q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h], scale, causal)
+            a, bk, bv = attention_backward_head(q[b, :, h], k[b, :, h // g], v[b, :, h // g], do[b, :, h], scale,
+                                                causal)
+            dq[b, :, h] = a
+            dk[b, :, h // g] += bk
+            dv[b, :, h // g] += bv
+    return dq, dk, dv
+
+
+def attention_backward_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool):
+    """Packed varlen backward: q, do [total_q, H, d], k, v [total_k, Hkv, d];
+    sequence s is rows cu[s]:cu[s+1] of each (bottom-right causal when the
+    lengths differ).  Rows outside every sequence stay 0."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    H = q.shape[1]
+    g = H // k.shape[1]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s in range(len(cu_seqlens_q) - 1):
+        qa, qb = int(cu_seqlens_q[s]), int(cu_seqlens_q[s + 1])
+        ka, kb = int(cu_seqlens_k[s]), int(cu_seqlens_k[s + 1])
+        for h in range(H):
+            a, bk, bv = attention_backward_head(q[qa:qb, h], k[ka:kb, h // g], v[ka:kb, h // g], do[qa:qb, h],
+                                                scale, causal)
+            dq[qa:qb, h] = a
+            dk[ka:kb, h // g] += bk
+            dv[ka:kb, h // g] += bv
     return dq, dk, dv

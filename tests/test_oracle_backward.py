@@ -1,5 +1,5 @@
-"""Pins for the oracle's backward pass (CPU only): attention_backward_head and
-attention_backward_dense.
+"""Pins for the oracle's backward pass (CPU only): attention_backward_head,
+attention_backward_dense and attention_backward_varlen.
 
 The checks never restate the chain rule the oracle uses.  They take the
 function under test as an argument, so the planted-mistake copies at the end
@@ -8,7 +8,9 @@ of this file run through the very same checks and must fail one of them:
 * central finite differences of L = sum(dO * O), with O from the forward
   oracle (pinned on its own elsewhere);
 * torch's float64 autograd through its own attention routine, for the
-  batched [B, N, H, d] layout;
+  batched [B, N, H, d] layout, grouped kv heads (expanded for torch, whose
+  autograd then sums each group) and varlen sequences with bottom-right
+  causal masking;
 * closed forms: with one key, O = v for every row, so dQ = dK = 0 and dV is
   the column sum of dO; since every row of dS sums to zero, the key gradients
   sum to zero over the keys and dQ does not change when one vector is added
@@ -146,3 +148,111 @@ def _mutant(kind):
                                   "dq_unscaled", "dk_from_do", "head_mixup"])
 def test_backward_mutant_is_caught(kind):
     assert check_backward(*_mutant(kind)) != []
+
+
+# ----------------------------------------------------------------- grouped heads and varlen
+
+
+def _torch_grads(q, k, v, do, scale, causal, group):
+    """torch float64 autograd of one sequence [L, H, d]; the kv heads are
+    expanded to the query heads, so autograd sums each group's gradients."""
+    tq, tk, tv = (torch.tensor(x.transpose(1, 0, 2), requires_grad=True) for x in (q, k, v))
+    Lq, Lk = q.shape[0], k.shape[0]
+    mask = None
+    if causal:
+        mask = torch.arange(Lk)[None, :] <= torch.arange(Lq)[:, None] + (Lk - Lq)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(group, 0), tv.repeat_interleave(group, 0), attn_mask=mask, scale=scale)
+    out.backward(torch.tensor(do.transpose(1, 0, 2)))
+    return [t.grad.numpy().transpose(1, 0, 2) for t in (tq, tk, tv)]
+
+
+def check_backward_wrappers(fn_dense, fn_varlen):
+    """Return the list of pins that the grouped dense / varlen wrappers fail."""
+    fails = []
+    rng = np.random.default_rng(302)
+    H, Hkv, d, scale = 6, 2, 8, 0.3
+    # Grouped dense: every sequence against torch autograd.
+    B, N = 2, 23
+    q, do = rng.normal(size=(B, N, H, d)), rng.normal(size=(B, N, H, d))
+    k, v = rng.normal(size=(B, N, Hkv, d)), rng.normal(size=(B, N, Hkv, d))
+    for causal in (False, True):
+        got = fn_dense(q, k, v, do, scale, causal)
+        for b in range(B):
+            want = _torch_grads(q[b], k[b], v[b], do[b], scale, causal, H // Hkv)
+            for name, a, w in zip(("dq", "dk", "dv"), got, want):
+                if not np.allclose(a[b], w, rtol=1e-10, atol=1e-12):
+                    fails.append(f"grouped dense {name} causal={causal}")
+    # Varlen with Lq <= Lk (bottom-right causal) and an empty sequence: each
+    # sequence against torch autograd on its own rows; rows between
+    # sequences' ends and the tensor end stay 0.
+    lq, lk = [5, 0, 17, 9], [9, 4, 17, 30]
+    cq = np.concatenate([[0], np.cumsum(lq)])
+    ck = np.concatenate([[0], np.cumsum(lk)])
+    q, do = rng.normal(size=(cq[-1], H, d)), rng.normal(size=(cq[-1], H, d))
+    k, v = rng.normal(size=(ck[-1], Hkv, d)), rng.normal(size=(ck[-1], Hkv, d))
+    for causal in (False, True):
+        gq, gk, gv = fn_varlen(q, k, v, do, cq, ck, scale, causal)
+        for s in range(len(lq)):
+            qs, ks = slice(cq[s], cq[s + 1]), slice(ck[s], ck[s + 1])
+            if lq[s] == 0:
+                if not (np.all(gk[ks] == 0) and np.all(gv[ks] == 0)):
+                    fails.append(f"varlen empty query sequence causal={causal}")
+                continue
+            want = _torch_grads(q[qs], k[ks], v[ks], do[qs], scale, causal, H // Hkv)
+            for name, a, w in zip(("dq", "dk", "dv"), (gq[qs], gk[ks], gv[ks]), want):
+                if not np.allclose(a, w, rtol=1e-10, atol=1e-12):
+                    fails.append(f"varlen {name} seq{s} causal={causal}")
+    return fails
+
+
+def test_backward_wrapper_pins():
+    assert check_backward_wrappers(oracle.attention_backward_dense, oracle.attention_backward_varlen) == []
+
+
+def _wrapper_mutant(kind):
+    def head_of(h, H, Hkv):
+        return h % Hkv if kind == "group_modulo" else h // (H // Hkv)
+
+    def dense(q, k, v, do, scale, causal):
+        B, N, H, d = q.shape
+        Hkv = k.shape[2]
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        for b in range(B):
+            for h in range(H):
+                hk = head_of(h, H, Hkv)
+                a, bk, bv = oracle.attention_backward_head(q[b, :, h], k[b, :, hk], v[b, :, hk], do[b, :, h], scale,
+                                                           causal)
+                dq[b, :, h] = a
+                if kind == "overwrite":
+                    dk[b, :, hk], dv[b, :, hk] = bk, bv
+                else:
+                    dk[b, :, hk] += bk
+                    dv[b, :, hk] += bv
+        return dq, dk, dv
+
+    def varlen(q, k, v, do, cq, ck, scale, causal):
+        H, Hkv = q.shape[1], k.shape[1]
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        for s in range(len(cq) - 1):
+            qa, qb, ka, kb = int(cq[s]), int(cq[s + 1]), int(ck[s]), int(ck[s + 1])
+            if kind == "top_left":  # causal aligned at the first key instead of the last
+                kb = ka + min(kb - ka, qb - qa) if causal else kb
+            for h in range(H):
+                hk = head_of(h, H, Hkv)
+                a, bk, bv = oracle.attention_backward_head(q[qa:qb, h], k[ka:kb, hk], v[ka:kb, hk], do[qa:qb, h],
+                                                           scale, causal)
+                dq[qa:qb, h] = a
+                if kind == "overwrite":
+                    dk[ka:kb, hk], dv[ka:kb, hk] = bk, bv
+                else:
+                    dk[ka:kb, hk] += bk
+                    dv[ka:kb, hk] += bv
+        return dq, dk, dv
+
+    return dense, varlen
+
+
+@pytest.mark.parametrize("kind", ["group_modulo", "overwrite", "top_left"])
+def test_backward_wrapper_mutant_is_caught(kind):
+    assert check_backward_wrappers(*_wrapper_mutant(kind)) != []
