@@ -31,7 +31,7 @@ EXPORTS = (
     "fa_abi_version", "fa_status_string", "fa_fwd", "fa_varlen_fwd", "fa_paged_workspace_size",
     "fa_paged_fwd", "fa_paged_fwd_noalloc", "fa_paged_gather", "fa_device_status", "fa_selftest_wait_timeout",
     "fa_varlen_paged_fwd", "fa_store_kvcache", "fa_qkvpacked_fwd", "fa_kvpacked_fwd", "fa_varlen_qkvpacked_fwd",
-    "fa_varlen_kvpacked_fwd",
+    "fa_varlen_kvpacked_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_varlen_bwd",
 )
 
 _lib = None
@@ -83,6 +83,13 @@ def load(path: str | None = None):
     lib.fa_paged_gather.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.fa_device_status.restype = i
     lib.fa_device_status.argtypes = [vp, i]
+    lib.fa_bwd_workspace_bytes.restype = sz
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+    lib.fa_varlen_bwd.restype = i
+    lib.fa_varlen_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, i, i, i, i, i, i, i, i, f, i,
+                                  vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp]
     _lib = lib
@@ -195,6 +202,25 @@ def fa_paged_gather(cache, block_table, seqlens, out, B, Hkv, d, page_size, num_
 
 def fa_device_status(stream=None, clear=True) -> int:
     return load().fa_device_status(_stream(stream), int(bool(clear)))
+
+
+def fa_bwd_workspace_bytes(num_seqs, total_q, H) -> int:
+    return load().fa_bwd_workspace_bytes(num_seqs, total_q, H)
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal,
+           stream=None) -> int:
+    return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                         _ptr(workspace), workspace_bytes, B, H, Hkv, N, d, scale, int(bool(causal)), _stream(stream))
+
+
+def fa_varlen_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, cu_seqlens_q, cu_seqlens_k,
+                  num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, H, Hkv, d, scale, causal,
+                  stream=None) -> int:
+    return load().fa_varlen_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(workspace), workspace_bytes, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, H, Hkv, d, scale,
+                                int(bool(causal)), _stream(stream))
 
 
 def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
@@ -354,3 +380,52 @@ def attention_kvpacked(q, kv, scale=None, causal=False, out=None, lse=None, stre
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _check(fa_kvpacked_fwd(q, kv, out, lse, B, H, Hkv, N, d, scale, causal, stream), "fa_kvpacked_fwd")
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, stream=None):
+    """Dense backward.  q, o, dout: [B, N, H, d]; k, v: [B, N, Hkv, d] bf16;
+    lse: [B, H, N] fp32 from the forward.  Returns (dq, dk, dv) bf16."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _req(t, name, torch.bfloat16)
+    _req(lse, "lse", torch.float32)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shapes: q, o, dout [B, N, H, d]; k, v [B, N, Hkv, d]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa_bwd_workspace_bytes(B, B * N, H)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace.numel() * workspace.element_size(), B, H,
+                Hkv, N, d, scale, causal, stream)
+    _check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def attention_varlen_backward(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                              scale=None, causal=False, workspace=None, stream=None):
+    """Varlen backward.  q, o, dout: [total_q, H, d]; k, v: [total_k, Hkv, d]
+    bf16; lse: [H, total_q] fp32.  Returns (dq, dk, dv) bf16."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _req(t, name, torch.bfloat16)
+    _req(lse, "lse", torch.float32)
+    _req(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _req(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+    total_q, H, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    num_seqs = cu_seqlens_q.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa_bwd_workspace_bytes(num_seqs, total_q, H)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = fa_varlen_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace.numel() * workspace.element_size(),
+                       cu_seqlens_q, cu_seqlens_k, num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, H, Hkv, d,
+                       scale, causal, stream)
+    _check(st, "fa_varlen_bwd")
+    return dq, dk, dv

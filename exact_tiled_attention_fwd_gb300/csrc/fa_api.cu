@@ -17,7 +17,7 @@ __device__ unsigned int g_fa_error_word;
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 constexpr int kMaxDevices = 64;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -519,6 +519,94 @@ int fa_selftest_wait_timeout(long long limit_ns, void* stream) {
     if (fa::launch_wait_selftest(err, static_cast<unsigned long long>(limit_ns), s) != cudaSuccess)
         return FA_ERR_CUDA;
     return FA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared body of fa_bwd and fa_varlen_bwd (cu_q == nullptr: dense).
+fa_status backward_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        const int* cu_q, const int* cu_k, int num_seqs, int N, int max_seqlen_q, int max_seqlen_k,
+                        int total_q, int total_k, int H, int Hkv, int d, float scale, int causal, void* stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return FA_ERR_INVALID;
+    if (cu_q && ((reinterpret_cast<uintptr_t>(cu_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_k) & 3u)))
+        return FA_ERR_INVALID;
+    if (num_seqs < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 ||
+        max_seqlen_k < 1 || !scale_ok(scale))
+        return FA_ERR_INVALID;
+    if (workspace_bytes < fa_bwd_workspace_bytes(num_seqs, total_q, H)) return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
+    unsigned int* err = nullptr;
+    fa_status st = ensure_init(&err);
+    if (st != FA_OK) return st;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((st = make_map(&tq, q, d, H, total_q)) != FA_OK) return st;
+    if ((st = make_map(&tk, k, d, Hkv, total_k)) != FA_OK) return st;
+    if ((st = make_map(&tv, v, d, Hkv, total_k)) != FA_OK) return st;
+    if ((st = make_map(&tdo, dout, d, H, total_q)) != FA_OK) return st;
+    fa::BackwardParams p{};
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.ws = static_cast<float*>(workspace);
+    p.ws_head_stride = fa::bwd_ws_head_stride(total_q, num_seqs);
+    p.cu_q = cu_q;
+    p.cu_k = cu_k;
+    p.N = N;
+    p.num_seqs = num_seqs;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
+    p.max_seqlen_q = max_seqlen_q;
+    p.max_seqlen_k = max_seqlen_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.num_q_blocks = (max_seqlen_q + fa::kBlockM - 1) / fa::kBlockM;
+    p.num_k_blocks = (max_seqlen_k + fa::kBlockN - 1) / fa::kBlockN;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.lse_head_stride = cu_q ? total_q : N;
+    p.err = err;
+    p.wait_limit_ns = wait_limit_ns();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(fa::launch_backward(tq, tk, tv, tdo, p, d, causal != 0, s), s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_bwd_workspace_bytes(int num_seqs, int total_q, int H) {
+    if (num_seqs < 1 || total_q < 0 || H < 1) return 0;
+    return 2 * static_cast<size_t>(H) * static_cast<size_t>(fa::bwd_ws_head_stride(total_q, num_seqs)) * sizeof(float);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+           void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+           float scale, int causal, void* stream) {
+    if (B < 1 || N < 1) return FA_ERR_INVALID;
+    const long long rows = static_cast<long long>(B) * N;
+    if (rows > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;
+    return backward_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, nullptr, nullptr, B, N, N, N,
+                         static_cast<int>(rows), static_cast<int>(rows), H, Hkv, d, scale, causal, stream);
+}
+
+int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q,
+                  int total_k, int H, int Hkv, int d, float scale, int causal, void* stream) {
+    if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID;
+    return backward_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, cu_seqlens_q, cu_seqlens_k,
+                         num_seqs, 0, max_seqlen_q, max_seqlen_k, total_q, total_k, H, Hkv, d, scale, causal, stream);
 }
 
 }  // extern "C"

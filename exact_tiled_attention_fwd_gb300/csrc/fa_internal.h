@@ -90,6 +90,48 @@ struct StoreParams {
 };
 cudaError_t launch_store_kvcache(const StoreParams& p, cudaStream_t stream);
 
+// Backward pass (dense or varlen, multi-head or grouped-query).
+//   q, o, dout, dq : bf16 [rows_q, H, d];  k, v, dk, dv : bf16 [rows_k, Hkv, d]
+//   lse            : the forward's fp32 LSE ([B, H, N] dense, [H, total_q] varlen)
+//   ws             : fp32 workspace, two arrays of H * ws_head_stride floats:
+//                    [0] the LSE in log2 units and [1] delta_i = dO_i . O_i,
+//                    sequence s's rows at bwd_ws_seq_offset(cu_q[s], s) of each
+//                    head, padded to a multiple of kBlockM rows (+inf / 0)
+struct BackwardParams {
+    const void* o;
+    const void* dout;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* ws;
+    long long ws_head_stride;
+    const int* cu_q;         // varlen: int32 [num_seqs + 1]; null for dense
+    const int* cu_k;
+    int N, num_seqs, H, Hkv, group;
+    int max_seqlen_q, max_seqlen_k, total_q, total_k;
+    int num_q_blocks, num_k_blocks;  // ceil(max_seqlen / 128)
+    float scale, scale_log2;
+    long long lse_head_stride;
+    unsigned int* err;
+    unsigned long long wait_limit_ns;
+};
+
+// First workspace row of sequence s (q_start = its first query row): a
+// multiple of 4 floats (16 bytes), and far enough from sequence s-1's rows
+// to hold them padded to kBlockM.
+__host__ __device__ inline long long bwd_ws_seq_offset(long long q_start, int s) {
+    return ((q_start + 3) & ~3ll) + 132ll * s;
+}
+inline long long bwd_ws_head_stride(long long total_q, int num_seqs) {
+    return (total_q + 132ll * num_seqs + 8 + 3) & ~3ll;
+}
+
+// Prep (delta, log2 LSE), then the dK/dV and dQ kernels, on one stream.
+cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BackwardParams& p, int d, bool causal,
+                            cudaStream_t stream);
+
 // Size of the fixed device scratch used by fa_paged_fwd_noalloc, and the
 // per-device lookup of its address (first call on a device does the lookup).
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;

@@ -248,6 +248,53 @@ int fa_paged_gather(const void* cache, const int* block_table, const int* seqlen
                     int max_pages_per_seq, int max_seqlen, void* stream);
 
 /*
+ * Backward pass: the gradients dQ, dK, dV of a loss with respect to the
+ * inputs of the forward, given dO.  P is recomputed from the forward's LSE
+ * (it is never stored), then
+ *
+ *     dV = P^T dO,   dP = dO V^T,   dS_ij = P_ij (dP_ij - delta_i),
+ *     delta_i = dO_i . O_i,   dQ = scale dS K,   dK = scale dS^T Q
+ *
+ * (the recomputation and the row-sum term of the lqnn.cn FlashAttention
+ * article, §2.3 and §4.3, and of the yulong.wang page, §2.3).  With grouped
+ * query heads, dK and dV of a kv head sum over its H / Hkv query heads.
+ * dQ is accumulated on chip per 128-row query block and written once (no
+ * atomics): the result is deterministic.
+ *
+ *   q, o, dout, dq : [B, N, H, d]   bf16   (o and lse: this library's forward
+ *   k, v, dk, dv   : [B, N, Hkv, d] bf16    output for the same q, k, v,
+ *   lse            : [B, H, N]      fp32    scale and causal)
+ *   workspace      : DEVICE memory of at least
+ *                    fa_bwd_workspace_bytes(B, B * N, H) bytes, 16-byte
+ *                    aligned, owned by the caller; its contents on entry do
+ *                    not matter and are overwritten.
+ * Rows whose LSE is -inf (no visible key) contribute nothing; keys that no
+ * query sees get dK = dV = 0.  Every row of dq, dk, dv is written.  Launches
+ * three kernels on `stream`.  Errors as for fa_fwd; a workspace smaller than
+ * required is FA_ERR_INVALID.
+ */
+size_t fa_bwd_workspace_bytes(int num_seqs, int total_q, int H);
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, void* workspace,
+           size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale,
+           int causal, void* stream);
+
+/*
+ * Varlen backward: the packed layouts of fa_varlen_fwd (q, o, dout, dq:
+ * [total_q, H, d]; k, v, dk, dv: [total_k, Hkv, d]; lse: [H, total_q];
+ * cu_seqlens_*: int32 DEVICE [num_seqs + 1]), workspace of
+ * fa_bwd_workspace_bytes(num_seqs, total_q, H) bytes.  Bottom-right causal as
+ * in the forward.  A bad cu_seqlens entry skips that sequence (its outputs
+ * are left untouched) and is reported by fa_device_status().
+ */
+int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                  size_t workspace_bytes, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                  int H, int Hkv, int d, float scale, int causal, void* stream);
+
+/*
  * Synchronise the stream, read the device error word and return FA_OK,
  * FA_ERR_TIMEOUT or FA_ERR_DEVICE_INDEX (or FA_ERR_CUDA if the sync itself
  * failed).  clear != 0 resets the word afterwards.

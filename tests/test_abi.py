@@ -51,7 +51,7 @@ def test_status_strings(lib):
     for code in range(6):
         assert lib.status_string(code).startswith("FA_")
     assert "unknown" in lib.status_string(99)
-    assert lib.fa_abi_version() == 3
+    assert lib.fa_abi_version() == 4
 
 
 def test_validation_without_gpu(lib):
