@@ -507,6 +507,7 @@ int fa_device_status(void* stream, int clear) {
     }
     if (word & FA_DEVERR_TIMEOUT) return FA_ERR_TIMEOUT;
     if (word & FA_DEVERR_INDEX) return FA_ERR_DEVICE_INDEX;
+    if (word & FA_DEVERR_LAYOUT) return FA_ERR_CUDA;
     return FA_OK;
 }
 

@@ -55,11 +55,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-__device__ __forceinline__ float4 ldg_nc_f4(const float* p) {
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     float4 r;
-    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-                 : "l"(p));
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr));
     return r;
 }
 
@@ -160,27 +158,43 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BackwardParams p) {
 // 32 (w % 4) .. + 31 and query columns 64 ((w - 4) / 4) .. + 63, so two
 // threads share a key row.  Their dS^T bf16 pairs go to the first 32 of
 // their own 64 dP^T columns, never into columns the other thread reads.
+//
+// Q_n and dO_n have rings of their own, each filled by its own producer
+// thread (warp 0 and warp 2), so that neither waits behind the other's
+// slot: a Q slot is freed by dK (the last product of a step), a dO slot
+// by dV.  lse2 and delta of the step's 128 query rows travel with Q_n (one
+// bulk copy each into a small buffer beside the Q slot); the compute warps
+// read them from shared memory, and the slot is only freed after dK, i.e.
+// after the compute warps have finished the step.
 template <int D>
 struct DkdvSmem {
     static constexpr uint32_t kTile = 128 * D * 2;      // a K, V, Q or dO tile
     static constexpr uint32_t kPTile = 128 * 128 * 2;   // P^T
-    static constexpr int kSlots = D == 128 ? 4 : 8;     // Q/dO ring (even: Q, odd: dO)
+    static constexpr int kSlots = D == 128 ? 2 : 4;     // per ring (Q, dO)
+    static constexpr uint32_t kAux = 1024;              // lse2[128], delta[128] (fp32)
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kK + kTile;
     static constexpr uint32_t kP = kV + kTile;
-    static constexpr uint32_t kRing = kP + kPTile;
-    static constexpr uint32_t kBar = kRing + kSlots * kTile;
-    static constexpr uint32_t kNumBars = 32;
+    static constexpr uint32_t kQR = kP + kPTile;
+    static constexpr uint32_t kDR = kQR + kSlots * kTile;
+    static constexpr uint32_t kAuxR = kDR + kSlots * kTile;
+    static constexpr uint32_t kBar = kAuxR + kSlots * kAux;
+    static constexpr uint32_t kNumBars = 26;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kUsed = kAbort + 4;
-    static constexpr uint32_t kDyn = (kUsed + 1024) > 118784u ? (kUsed + 1024) : 118784u;
+    // No alignment slack: the kernel checks that the dynamic shared memory
+    // starts on a 1024-byte boundary (the 128-byte swizzle atom) and reports
+    // FA_DEVERR_LAYOUT otherwise.  At least 116 KiB so one CTA holds an SM.
+    static constexpr uint32_t kDyn = kUsed > 118784u ? kUsed : 118784u;
 };
 
 enum DkdvBar : uint32_t {
     A_KV_FULL = 0,
-    A_FULL = 1,       // + slot (8)
-    A_EMPTY = 9,      // + slot (8)
+    A_Q_FULL = 1,     // + slot (4): Q_n, lse2_n, delta_n
+    A_Q_EMPTY = 5,    // + slot (4)
+    A_DO_FULL = 9,    // + slot (4)
+    A_DO_EMPTY = 13,  // + slot (4)
     A_S_FULL = 17,    // S^T_n in TMEM
     A_S_FREE = 18,    // compute warps have read S^T_n (8 arrivals)
     A_DP_FULL = 19,   // dP^T_n in TMEM
@@ -204,9 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdescT = idesc_bf16_f32(128, 128, false);  // S^T, dP^T
     constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, true);     // dV, dK
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
+    if (sbase & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.err, FA_DEVERR_LAYOUT);
+        return;
+    }
     auto bar = [&](uint32_t id) { return sbase + L::kBar + id * 8; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
@@ -268,42 +286,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(128 * kRegsLow + 256 * kRegsHigh <= 168 * kThreads, "register split exceeds the launch");
     if (warp < 4) {
         regs_dec<kRegsLow>();
-        if (warp == 0) {
-            // ================= TMA producer =================
+        if (warp == 0 || warp == 2) {
+            // ================= TMA producers: warp 0 K, V, then Q_n (+ lse2,
+            // delta); warp 2 dO_n =================
+            const bool is_q = warp == 0;
             if (lane == 0) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_k);
-                tma_prefetch_desc(&tm_v);
-                tma_prefetch_desc(&tm_do);
-                mbar_arrive_expect_tx(bar(A_KV_FULL), 2 * L::kTile);
+                const uint32_t ring_full = is_q ? A_Q_FULL : A_DO_FULL;
+                const uint32_t ring_empty = is_q ? A_Q_EMPTY : A_DO_EMPTY;
+                const uint32_t ring = is_q ? L::kQR : L::kDR;
+                const void* map = is_q ? static_cast<const void*>(&tm_q) : static_cast<const void*>(&tm_do);
+                tma_prefetch_desc(map);
+                if (is_q) {
+                    tma_prefetch_desc(&tm_k);
+                    tma_prefetch_desc(&tm_v);
+                    mbar_arrive_expect_tx(bar(A_KV_FULL), 2 * L::kTile);
 #pragma unroll
-                for (int pn = 0; pn < kPanels; ++pn) {
-                    tma_load_3d(sbase + L::kK + pn * kPanelBytes, &tm_k, bar(A_KV_FULL), pn * 64, hk,
-                                g.k_start + key0);
-                    tma_load_3d(sbase + L::kV + pn * kPanelBytes, &tm_v, bar(A_KV_FULL), pn * 64, hk,
-                                g.k_start + key0);
+                    for (int pn = 0; pn < kPanels; ++pn) {
+                        tma_load_3d(sbase + L::kK + pn * kPanelBytes, &tm_k, bar(A_KV_FULL), pn * 64, hk,
+                                    g.k_start + key0);
+                        tma_load_3d(sbase + L::kV + pn * kPanelBytes, &tm_v, bar(A_KV_FULL), pn * 64, hk,
+                                    g.k_start + key0);
+                    }
                 }
-                // Ring tile t: Q of step t/2 (t even) or dO of step t/2 (t odd).
+                const float* ws_seq = p.ws + bwd_ws_seq_offset(g.q_start, seq);
                 bool ok = true;
-                const int n_tiles = 2 * n_steps;
-                for (int t = 0; ok && t < n_tiles; ++t) {
-                    const int s = t % kSlots;
-                    if (t >= kSlots) ok = mbar_wait(bar(A_EMPTY + s), ((t / kSlots) - 1) & 1, abort_flag, p.err, lim);
+                for (int n = 0; ok && n < n_steps; ++n) {
+                    const int s = n % kSlots;
+                    if (n >= kSlots) ok = mbar_wait(bar(ring_empty + s), ((n / kSlots) - 1) & 1, abort_flag, p.err, lim);
                     if (!ok) break;
-                    const int n = t >> 1;
-                    const void* map = (t & 1) ? static_cast<const void*>(&tm_do) : static_cast<const void*>(&tm_q);
-                    mbar_arrive_expect_tx(bar(A_FULL + s), L::kTile);
+                    const int hq = step_head(n), ib = step_block(n);
+                    mbar_arrive_expect_tx(bar(ring_full + s), L::kTile + (is_q ? 1024u : 0u));
 #pragma unroll
                     for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + L::kRing + s * L::kTile + pn * kPanelBytes, map, bar(A_FULL + s), pn * 64,
-                                    step_head(n), g.q_start + step_block(n) * kBlockM);
+                        tma_load_3d(sbase + ring + s * L::kTile + pn * kPanelBytes, map, bar(ring_full + s), pn * 64,
+                                    hq, g.q_start + ib * kBlockM);
+                    if (is_q) {
+                        const float* src = ws_seq + hq * p.ws_head_stride + ib * kBlockM;
+                        bulk_load_1d(sbase + L::kAuxR + s * L::kAux, src, 512, bar(ring_full + s));
+                        bulk_load_1d(sbase + L::kAuxR + s * L::kAux + 512, src + p.H * p.ws_head_stride, 512,
+                                     bar(ring_full + s));
+                    }
                 }
-                // Drain: every copy issued lands before the CTA exits.
-                mbar_wait_drain(bar(A_KV_FULL), 0, lim);
-                for (int s = 0; s < kSlots; ++s) {
-                    if (s >= n_tiles) break;
-                    const int last = s + ((n_tiles - 1 - s) / kSlots) * kSlots;  // last tile put in slot s
-                    mbar_wait_drain(bar(A_FULL + s), (last / kSlots) & 1, lim);
+                // Drain: every copy this thread issued lands before the CTA exits.
+                if (is_q) mbar_wait_drain(bar(A_KV_FULL), 0, lim);
+                for (int s = 0; s < kSlots && s < n_steps; ++s) {
+                    const int last = s + ((n_steps - 1 - s) / kSlots) * kSlots;  // last step put in slot s
+                    mbar_wait_drain(bar(ring_full + s), (last / kSlots) & 1, lim);
                 }
             }
             __syncwarp();
@@ -312,17 +340,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dk_a = sdesc_sw128(sbase + L::kK, 16, 1024);
             const uint64_t dv_a = sdesc_sw128(sbase + L::kV, 16, 1024);
             const uint64_t dp_a = sdesc_sw128(sbase + L::kP, 16, 1024);
-            const uint64_t ring_k = sdesc_sw128(sbase + L::kRing, 16, 1024);           // Q / dO as K-major B
-            const uint64_t ring_mn = sdesc_sw128(sbase + L::kRing, kPanelBytes, 1024);  // Q / dO as MN-major B
+            const uint64_t q_k = sdesc_sw128(sbase + L::kQR, 16, 1024);             // Q as K-major B
+            const uint64_t q_mn = sdesc_sw128(sbase + L::kQR, kPanelBytes, 1024);   // Q as MN-major B
+            const uint64_t do_k = sdesc_sw128(sbase + L::kDR, 16, 1024);
+            const uint64_t do_mn = sdesc_sw128(sbase + L::kDR, kPanelBytes, 1024);
             const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 384;
             bool ok = warp_wait(bar(A_KV_FULL), 0, abort_flag, p.err, lim);
-            auto wait_tile = [&](int t) {
-                ok = ok && warp_wait(bar(A_FULL + t % kSlots), (t / kSlots) & 1, abort_flag, p.err, lim);
+            auto wait_q = [&](int n) {
+                ok = ok && warp_wait(bar(A_Q_FULL + n % kSlots), (n / kSlots) & 1, abort_flag, p.err, lim);
             };
-            auto slot_off = [&](int t) { return static_cast<uint32_t>(((t % kSlots) * L::kTile) >> 4); };
+            auto wait_do = [&](int n) {
+                ok = ok && warp_wait(bar(A_DO_FULL + n % kSlots), (n / kSlots) & 1, abort_flag, p.err, lim);
+            };
+            auto slot_off = [&](int n) { return static_cast<uint32_t>(((n % kSlots) * L::kTile) >> 4); };
             // S^T_n = K Q_n^T
             auto issue_s = [&](int n) {
-                const uint64_t b0 = ring_k + slot_off(2 * n);
+                const uint64_t b0 = q_k + slot_off(n);
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
@@ -333,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // dP^T_n = V dO_n^T
             auto issue_dp = [&](int n) {
-                const uint64_t b0 = ring_k + slot_off(2 * n + 1);
+                const uint64_t b0 = do_k + slot_off(n);
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
@@ -344,41 +377,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // dV += P^T_n dO_n (dO_n as N = d x K = 128 queries, MN-major)
             auto issue_dv = [&](int n) {
-                const uint64_t b0 = ring_mn + slot_off(2 * n + 1);
+                const uint64_t b0 = do_mn + slot_off(n);
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < 128 / 16; ++kk)
                         mma_ss(t_dv, dp_a + kmajor_step(kk), b0 + ((kk * 16 * 128) >> 4), kIdescG,
                                (n > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar(A_P_EMPTY));
-                    tc_commit(bar(A_EMPTY + (2 * n + 1) % kSlots));
+                    tc_commit(bar(A_DO_EMPTY + n % kSlots));
                 }
                 __syncwarp();
             };
             // dK += dS^T_n Q_n, dS^T from TMEM: queries 16 kk .. 16 kk + 15 are
             // 8 columns at 128 + 64 (kk / 4) + 8 (kk % 4)
             auto issue_dk = [&](int n) {
-                const uint64_t b0 = ring_mn + slot_off(2 * n);
+                const uint64_t b0 = q_mn + slot_off(n);
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < 128 / 16; ++kk)
                         mma_ts(t_dk, t_dp + 64 * (kk >> 2) + 8 * (kk & 3), b0 + ((kk * 16 * 128) >> 4), kIdescG,
                                (n > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar(A_DS_EMPTY));
-                    tc_commit(bar(A_EMPTY + (2 * n) % kSlots));
+                    tc_commit(bar(A_Q_EMPTY + n % kSlots));
                     if (n == n_steps - 1) tc_commit(bar(A_DONE));
                 }
                 __syncwarp();
             };
-            wait_tile(0);
+            wait_q(0);
             if (ok) issue_s(0);
-            wait_tile(1);
+            wait_do(0);
             if (ok) issue_dp(0);
             for (int n = 0; ok && n < n_steps; ++n) {
                 if (n + 1 < n_steps) {
                     // S^T_{n+1} overwrites S^T_n: the compute warps have read it.
                     ok = ok && warp_wait(bar(A_S_FREE), n & 1, abort_flag, p.err, lim);
-                    wait_tile(2 * n + 2);
+                    wait_q(n + 1);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(n + 1);
@@ -394,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n + 1 < n_steps) {
                     // dP^T_{n+1} overwrites dS^T_n: dK has read it.
                     ok = ok && warp_wait(bar(A_DS_EMPTY), n & 1, abort_flag, p.err, lim);
-                    wait_tile(2 * n + 3);
+                    wait_do(n + 1);
                     if (!ok) break;
                     tc_fence_after();
                     issue_dp(n + 1);
@@ -426,22 +459,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t c_s = 64 * half, c_dp = 128 + 64 * half;
     const uint32_t p_row = sbase + L::kP + half * kPanelBytes + r * 128;
     const uint32_t p_sw = static_cast<uint32_t>(r & 7);
-    const float c = p.scale_log2;
-    const float* ws_l2 = p.ws + bwd_ws_seq_offset(g.q_start, seq) + 64 * half;
-    const float* ws_dl = ws_l2 + p.H * p.ws_head_stride;
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int n = 0; ok && n < n_steps; ++n) {
-        const int hq = step_head(n), ib = step_block(n);
-        const long long woff = hq * p.ws_head_stride + ib * kBlockM;
-        if (!warp_wait(bar(A_S_FULL), n & 1, abort_flag, p.err, lim)) {
+        const int ib = step_block(n);
+        // lse2 / delta of this thread's 64 query columns (they landed with Q_n,
+        // whose barrier S^T_n's product already waited on)
+        const uint32_t aux = sbase + L::kAuxR + (n % kSlots) * L::kAux + 256 * half;
+        if (!warp_wait(bar(A_S_FULL), n & 1, abort_flag, p.err, lim) ||
+            !warp_wait(bar(A_Q_FULL + n % kSlots), (n / kSlots) & 1, abort_flag, p.err, lim)) {
             ok = false;
             break;
         }
         tc_fence_after();
         // P^T = 2^(S^T c - lse2); causal: query q sees this key iff q >= key - diag,
-        // i.e. local column cl < lo is masked.
-        float pv[64];
+        // i.e. local column cl < lo is masked (only near the diagonal).
+        float2 pv[32];
         const int lo = CAUSAL ? key - diag - ib * kBlockM - 64 * half : -1;
+        const bool masked = CAUSAL && __any_sync(0xffffffffu, lo > 0);
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
             uint32_t w[32];
@@ -454,14 +489,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 l = ldg_nc_f4(ws_l2 + woff + 32 * ch + 4 * q4);
-                const float la[4] = {l.x, l.y, l.z, l.w};
+                const float4 l = ld_shared_f4(aux + 4 * (32 * ch + 4 * q4));
+                const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(w[4 * q4]), __uint_as_float(w[4 * q4 + 1])),
+                                             c2, make_float2(-l.x, -l.y));
+                const float2 x1 = __ffma2_rn(
+                    make_float2(__uint_as_float(w[4 * q4 + 2]), __uint_as_float(w[4 * q4 + 3])), c2,
+                    make_float2(-l.z, -l.w));
+                pv[16 * ch + 2 * q4] = make_float2(ex2(x0.x), ex2(x0.y));
+                pv[16 * ch + 2 * q4 + 1] = make_float2(ex2(x1.x), ex2(x1.y));
+            }
+        }
+        if (masked) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int cl = 32 * ch + 4 * q4 + e;
-                    const float x = ex2(fmaf(__uint_as_float(w[4 * q4 + e]), c, -la[e]));
-                    pv[cl] = (CAUSAL && cl < lo) ? 0.f : x;
-                }
+            for (int i = 0; i < 32; ++i) {
+                if (2 * i < lo) pv[i].x = 0.f;
+                if (2 * i + 1 < lo) pv[i].y = 0.f;
             }
         }
         // dV of step n-1 has read the P^T tile.
@@ -472,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
             const uint32_t addr = p_row + ((static_cast<uint32_t>(cc) ^ p_sw) << 4);
-            st_shared_v4(addr, pack_bf16x2(pv[8 * cc], pv[8 * cc + 1]), pack_bf16x2(pv[8 * cc + 2], pv[8 * cc + 3]),
-                         pack_bf16x2(pv[8 * cc + 4], pv[8 * cc + 5]), pack_bf16x2(pv[8 * cc + 6], pv[8 * cc + 7]));
+            st_shared_v4(addr, pack_bf16x2(pv[4 * cc].x, pv[4 * cc].y), pack_bf16x2(pv[4 * cc + 1].x, pv[4 * cc + 1].y),
+                         pack_bf16x2(pv[4 * cc + 2].x, pv[4 * cc + 2].y), pack_bf16x2(pv[4 * cc + 3].x, pv[4 * cc + 3].y));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -491,12 +533,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(t_row + c_dp + 32 * ch, w);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 dl = ldg_nc_f4(ws_dl + woff + 32 * ch + 4 * q4);
-                const int cl = 32 * ch + 4 * q4;
-                pk[cl / 2] = pack_bf16x2(pv[cl] * (__uint_as_float(w[4 * q4]) - dl.x),
-                                         pv[cl + 1] * (__uint_as_float(w[4 * q4 + 1]) - dl.y));
-                pk[cl / 2 + 1] = pack_bf16x2(pv[cl + 2] * (__uint_as_float(w[4 * q4 + 2]) - dl.z),
-                                             pv[cl + 3] * (__uint_as_float(w[4 * q4 + 3]) - dl.w));
+                const float4 dl = ld_shared_f4(aux + 512 + 4 * (32 * ch + 4 * q4));
+                const int i = 16 * ch + 2 * q4;
+                const float2 a = __fmul2_rn(pv[i], __fadd2_rn(make_float2(__uint_as_float(w[4 * q4]),
+                                                                          __uint_as_float(w[4 * q4 + 1])),
+                                                              make_float2(-dl.x, -dl.y)));
+                const float2 b = __fmul2_rn(pv[i + 1], __fadd2_rn(make_float2(__uint_as_float(w[4 * q4 + 2]),
+                                                                              __uint_as_float(w[4 * q4 + 3])),
+                                                                  make_float2(-dl.z, -dl.w)));
+                pk[i] = pack_bf16x2(a.x, a.y);
+                pk[i + 1] = pack_bf16x2(b.x, b.y);
             }
         }
         tmem_st32(t_row + c_dp, pk);
@@ -652,47 +698,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(128 * kRegsLow + 256 * kRegsHigh <= 168 * kThreads, "register split exceeds the launch");
     if (warp < 4) {
         regs_dec<kRegsLow>();
-        if (warp == 0) {
-            // ================= TMA producer =================
+        if (warp == 0 || warp == 2) {
+            // ================= TMA producers: warp 0 Q, dO and the K ring;
+            // warp 2 the V ring =================
+            const bool is_k = warp == 0;
             if (lane == 0) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_k);
-                tma_prefetch_desc(&tm_v);
-                tma_prefetch_desc(&tm_do);
-                mbar_arrive_expect_tx(bar(B_QD_FULL), 2 * L::kTile);
+                const int nslots = is_k ? kKS : kVS;
+                const uint32_t full = is_k ? B_K_FULL : B_V_FULL, empty = is_k ? B_K_EMPTY : B_V_EMPTY;
+                const uint32_t ring = is_k ? L::kKR : L::kVR;
+                const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
+                tma_prefetch_desc(map);
+                if (is_k) {
+                    tma_prefetch_desc(&tm_q);
+                    tma_prefetch_desc(&tm_do);
+                    mbar_arrive_expect_tx(bar(B_QD_FULL), 2 * L::kTile);
 #pragma unroll
-                for (int pn = 0; pn < kPanels; ++pn) {
-                    tma_load_3d(sbase + L::kQ + pn * kPanelBytes, &tm_q, bar(B_QD_FULL), pn * 64, h, g.q_start + row0);
-                    tma_load_3d(sbase + L::kDO + pn * kPanelBytes, &tm_do, bar(B_QD_FULL), pn * 64, h,
-                                g.q_start + row0);
+                    for (int pn = 0; pn < kPanels; ++pn) {
+                        tma_load_3d(sbase + L::kQ + pn * kPanelBytes, &tm_q, bar(B_QD_FULL), pn * 64, h,
+                                    g.q_start + row0);
+                        tma_load_3d(sbase + L::kDO + pn * kPanelBytes, &tm_do, bar(B_QD_FULL), pn * 64, h,
+                                    g.q_start + row0);
+                    }
                 }
                 bool ok = true;
                 for (int j = 0; ok && j < n_steps; ++j) {
-                    const int ks = j % kKS, vs = j % kVS;
-                    if (j >= kKS) ok = mbar_wait(bar(B_K_EMPTY + ks), ((j / kKS) - 1) & 1, abort_flag, p.err, lim);
+                    const int sl = j % nslots;
+                    if (j >= nslots) ok = mbar_wait(bar(empty + sl), ((j / nslots) - 1) & 1, abort_flag, p.err, lim);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar(B_K_FULL + ks), L::kTile);
+                    mbar_arrive_expect_tx(bar(full + sl), L::kTile);
 #pragma unroll
                     for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + L::kKR + ks * L::kTile + pn * kPanelBytes, &tm_k, bar(B_K_FULL + ks),
-                                    pn * 64, hk, g.k_start + j * kBlockN);
-                    if (j >= kVS) ok = mbar_wait(bar(B_V_EMPTY + vs), ((j / kVS) - 1) & 1, abort_flag, p.err, lim);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(bar(B_V_FULL + vs), L::kTile);
-#pragma unroll
-                    for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + L::kVR + vs * L::kTile + pn * kPanelBytes, &tm_v, bar(B_V_FULL + vs),
-                                    pn * 64, hk, g.k_start + j * kBlockN);
+                        tma_load_3d(sbase + ring + sl * L::kTile + pn * kPanelBytes, map, bar(full + sl), pn * 64, hk,
+                                    g.k_start + j * kBlockN);
                 }
-                // Drain: the last fill of every slot, and Q / dO.
-                mbar_wait_drain(bar(B_QD_FULL), 0, lim);
-                for (int s = 0; s < kKS && s < n_steps; ++s) {
-                    const int last = s + ((n_steps - 1 - s) / kKS) * kKS;
-                    mbar_wait_drain(bar(B_K_FULL + s), (last / kKS) & 1, lim);
-                }
-                for (int s = 0; s < kVS && s < n_steps; ++s) {
-                    const int last = s + ((n_steps - 1 - s) / kVS) * kVS;
-                    mbar_wait_drain(bar(B_V_FULL + s), (last / kVS) & 1, lim);
+                // Drain: the last fill of every slot (and Q / dO).
+                if (is_k) mbar_wait_drain(bar(B_QD_FULL), 0, lim);
+                for (int sl = 0; sl < nslots && sl < n_steps; ++sl) {
+                    const int last = sl + ((n_steps - 1 - sl) / nslots) * nslots;
+                    mbar_wait_drain(bar(full + sl), (last / nslots) & 1, lim);
                 }
             }
             __syncwarp();
@@ -790,11 +833,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // query row of the block == TMEM lane
     const int row = row0 + r;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float c = p.scale_log2;
-    const float NEG_INF = -__int_as_float(0x7f800000);
     const long long woff = h * p.ws_head_stride + bwd_ws_seq_offset(g.q_start, seq) + row;
     const float lse2 = p.ws[woff];                              // padded rows: +inf
     const float delta = p.ws[woff + p.H * p.ws_head_stride];    // padded rows: 0
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+    const float2 nl2 = make_float2(-lse2, -lse2);
+    const float2 nd2 = make_float2(-delta, -delta);
     bool ok = true;
     for (int j = 0; ok && j < n_steps; ++j) {
         const uint32_t c_s = 128 * (j & 1) + 64 * half;
@@ -806,14 +850,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t u[64];
         tmem_ld64(t_row + c_s, u);
         // keys past the sequence, and (causal) keys past row + diag, get P = 0
+        // (only blocks that reach past the sequence end or the diagonal)
         const int kbase = j * kBlockN + 64 * half;
         int lim_c = g.Lk - 1 - kbase;
         if (CAUSAL) lim_c = min(lim_c, row + diag - kbase);
-        float pv[64];
+        const bool masked = __any_sync(0xffffffffu, lim_c < 63);
+        float2 pv[32];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            const float x = (i > lim_c) ? NEG_INF : fmaf(__uint_as_float(u[i]), c, -lse2);
-            pv[i] = ex2(x);
+        for (int i = 0; i < 32; ++i) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2, nl2);
+            pv[i] = make_float2(ex2(x.x), ex2(x.y));
+        }
+        if (masked) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                if (2 * i > lim_c) pv[i].x = 0.f;
+                if (2 * i + 1 > lim_c) pv[i].y = 0.f;
+            }
         }
         if (!warp_wait(bar(B_DP_FULL), j & 1, abort_flag, p.err, lim)) {
             ok = false;
@@ -826,9 +879,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_DP_FREE));
         uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            pk[i] = pack_bf16x2(pv[2 * i] * (__uint_as_float(u[2 * i]) - delta),
-                                pv[2 * i + 1] * (__uint_as_float(u[2 * i + 1]) - delta));
+        for (int i = 0; i < 32; ++i) {
+            const float2 ds = __fmul2_rn(pv[i], __fadd2_rn(make_float2(__uint_as_float(u[2 * i]),
+                                                                        __uint_as_float(u[2 * i + 1])), nd2));
+            pk[i] = pack_bf16x2(ds.x, ds.y);
+        }
         tmem_st32(t_row + c_s, pk);
         tmem_st_wait();
         tc_fence_before();
@@ -866,7 +921,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_dc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                       const BackwardParams& p, cudaStream_t stream) {
     static_assert(DkdvSmem<D>::kDyn <= 232448u && DqSmem<D>::kDyn <= 232448u, "shared memory budget");
-    static_assert(DkdvSmem<D>::kSlots <= 8 && DqSmem<D>::kKSlots <= 4 && DqSmem<D>::kVSlots <= 4, "barrier slots");
+    static_assert(DkdvSmem<D>::kSlots <= 4 && DqSmem<D>::kKSlots <= 4 && DqSmem<D>::kVSlots <= 4, "barrier slots");
     const dim3 gp(p.num_q_blocks, p.H, p.num_seqs);
     bwd_prep_kernel<D><<<gp, 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();

@@ -10,6 +10,7 @@
 // Bits of the device error word.
 #define FA_DEVERR_TIMEOUT 1u
 #define FA_DEVERR_INDEX 2u
+#define FA_DEVERR_LAYOUT 4u  // a kernel found its shared memory misaligned
 
 namespace fa {
 
