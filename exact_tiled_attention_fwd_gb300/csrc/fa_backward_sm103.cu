@@ -179,7 +179,7 @@ struct DkdvSmem {
     static constexpr uint32_t kDR = kQR + kSlots * kTile;
     static constexpr uint32_t kAuxR = kDR + kSlots * kTile;
     static constexpr uint32_t kBar = kAuxR + kSlots * kAux;
-    static constexpr uint32_t kNumBars = 26;
+    static constexpr uint32_t kNumBars = 28;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kUsed = kAbort + 4;
@@ -202,9 +202,9 @@ enum DkdvBar : uint32_t {
     A_P_EMPTY = 21,   // dV += P^T_n dO_n done
     A_DS_FULL = 22,   // dS^T_n in TMEM (8 arrivals)
     A_DS_EMPTY = 23,  // dK += dS^T_n Q_n done
-    A_DONE = 24,      // every MMA done: dK, dV final
-    A_DRAIN = 25,     // issuer's own drain before tensor memory is freed
-    A_COUNT = 26,
+    A_DONE = 24,      // + issuer (2): its last product done (dK, dV final)
+    A_DRAIN = 26,     // + issuer (2): own drain before tensor memory is freed
+    A_COUNT = 28,
 };
 
 template <int D, bool CAUSAL>
@@ -281,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto step_head = [&](int n) { return hk * p.group + n / per_head; };
     auto step_block = [&](int n) { return i_lo + n % per_head; };
 
-    // 128 * 88 + 256 * 208 = 64,512 = 384 * 168 (the launch's registers).
-    constexpr uint32_t kRegsLow = 88, kRegsHigh = 208;
+    // 128 * 72 + 256 * 216 = 64,512 = 384 * 168 (the launch's registers).
+    constexpr uint32_t kRegsLow = 72, kRegsHigh = 216;
     static_assert(128 * kRegsLow + 256 * kRegsHigh <= 168 * kThreads, "register split exceeds the launch");
     if (warp < 4) {
         regs_dec<kRegsLow>();
@@ -335,108 +335,117 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
-        } else if (warp == 1) {
-            // ================= MMA issuer =================
-            const uint64_t dk_a = sdesc_sw128(sbase + L::kK, 16, 1024);
-            const uint64_t dv_a = sdesc_sw128(sbase + L::kV, 16, 1024);
-            const uint64_t dp_a = sdesc_sw128(sbase + L::kP, 16, 1024);
-            const uint64_t q_k = sdesc_sw128(sbase + L::kQR, 16, 1024);             // Q as K-major B
-            const uint64_t q_mn = sdesc_sw128(sbase + L::kQR, kPanelBytes, 1024);   // Q as MN-major B
-            const uint64_t do_k = sdesc_sw128(sbase + L::kDR, 16, 1024);
-            const uint64_t do_mn = sdesc_sw128(sbase + L::kDR, kPanelBytes, 1024);
+        } else {
+            // ================= MMA issuers: warp 1 S^T and dK (the Q ring),
+            // warp 3 dP^T and dV (the dO ring).  Two issue streams keep the
+            // tensor pipe fed while either one waits. =================
             const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 384;
+            const int who = warp == 1 ? 0 : 1;
             bool ok = warp_wait(bar(A_KV_FULL), 0, abort_flag, p.err, lim);
-            auto wait_q = [&](int n) {
-                ok = ok && warp_wait(bar(A_Q_FULL + n % kSlots), (n / kSlots) & 1, abort_flag, p.err, lim);
-            };
-            auto wait_do = [&](int n) {
-                ok = ok && warp_wait(bar(A_DO_FULL + n % kSlots), (n / kSlots) & 1, abort_flag, p.err, lim);
-            };
             auto slot_off = [&](int n) { return static_cast<uint32_t>(((n % kSlots) * L::kTile) >> 4); };
-            // S^T_n = K Q_n^T
-            auto issue_s = [&](int n) {
-                const uint64_t b0 = q_k + slot_off(n);
-                if (elect_one()) {
+            if (who == 0) {
+                const uint64_t dk_a = sdesc_sw128(sbase + L::kK, 16, 1024);
+                const uint64_t q_k = sdesc_sw128(sbase + L::kQR, 16, 1024);             // Q as K-major B
+                const uint64_t q_mn = sdesc_sw128(sbase + L::kQR, kPanelBytes, 1024);   // Q as MN-major B
+                auto wait_q = [&](int n) {
+                    ok = ok && warp_wait(bar(A_Q_FULL + n % kSlots), (n / kSlots) & 1, abort_flag, p.err, lim);
+                };
+                // S^T_n = K Q_n^T
+                auto issue_s = [&](int n) {
+                    const uint64_t b0 = q_k + slot_off(n);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(t_s, dk_a + kmajor_step(kk), b0 + kmajor_step(kk), kIdescT, kk > 0 ? 1u : 0u);
-                    tc_commit(bar(A_S_FULL));
-                }
-                __syncwarp();
-            };
-            // dP^T_n = V dO_n^T
-            auto issue_dp = [&](int n) {
-                const uint64_t b0 = do_k + slot_off(n);
-                if (elect_one()) {
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss(t_s, dk_a + kmajor_step(kk), b0 + kmajor_step(kk), kIdescT, kk > 0 ? 1u : 0u);
+                        tc_commit(bar(A_S_FULL));
+                    }
+                    __syncwarp();
+                };
+                // dK += dS^T_n Q_n, dS^T from TMEM: queries 16 kk .. 16 kk + 15 are
+                // 8 columns at 128 + 64 (kk / 4) + 8 (kk % 4)
+                auto issue_dk = [&](int n) {
+                    const uint64_t b0 = q_mn + slot_off(n);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(t_dp, dv_a + kmajor_step(kk), b0 + kmajor_step(kk), kIdescT, kk > 0 ? 1u : 0u);
-                    tc_commit(bar(A_DP_FULL));
-                }
-                __syncwarp();
-            };
-            // dV += P^T_n dO_n (dO_n as N = d x K = 128 queries, MN-major)
-            auto issue_dv = [&](int n) {
-                const uint64_t b0 = do_mn + slot_off(n);
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < 128 / 16; ++kk)
-                        mma_ss(t_dv, dp_a + kmajor_step(kk), b0 + ((kk * 16 * 128) >> 4), kIdescG,
-                               (n > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar(A_P_EMPTY));
-                    tc_commit(bar(A_DO_EMPTY + n % kSlots));
-                }
-                __syncwarp();
-            };
-            // dK += dS^T_n Q_n, dS^T from TMEM: queries 16 kk .. 16 kk + 15 are
-            // 8 columns at 128 + 64 (kk / 4) + 8 (kk % 4)
-            auto issue_dk = [&](int n) {
-                const uint64_t b0 = q_mn + slot_off(n);
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < 128 / 16; ++kk)
-                        mma_ts(t_dk, t_dp + 64 * (kk >> 2) + 8 * (kk & 3), b0 + ((kk * 16 * 128) >> 4), kIdescG,
-                               (n > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar(A_DS_EMPTY));
-                    tc_commit(bar(A_Q_EMPTY + n % kSlots));
-                    if (n == n_steps - 1) tc_commit(bar(A_DONE));
-                }
-                __syncwarp();
-            };
-            wait_q(0);
-            if (ok) issue_s(0);
-            wait_do(0);
-            if (ok) issue_dp(0);
-            for (int n = 0; ok && n < n_steps; ++n) {
-                if (n + 1 < n_steps) {
-                    // S^T_{n+1} overwrites S^T_n: the compute warps have read it.
-                    ok = ok && warp_wait(bar(A_S_FREE), n & 1, abort_flag, p.err, lim);
-                    wait_q(n + 1);
+                        for (int kk = 0; kk < 128 / 16; ++kk)
+                            mma_ts(t_dk, t_dp + 64 * (kk >> 2) + 8 * (kk & 3), b0 + ((kk * 16 * 128) >> 4), kIdescG,
+                                   (n > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bar(A_DS_EMPTY));
+                        tc_commit(bar(A_Q_EMPTY + n % kSlots));
+                        if (n == n_steps - 1) tc_commit(bar(A_DONE));
+                    }
+                    __syncwarp();
+                };
+                wait_q(0);
+                if (ok) issue_s(0);
+                for (int n = 0; ok && n < n_steps; ++n) {
+                    if (n + 1 < n_steps) {
+                        // S^T_{n+1} overwrites S^T_n: the compute warps have read it.
+                        ok = ok && warp_wait(bar(A_S_FREE), n & 1, abort_flag, p.err, lim);
+                        wait_q(n + 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(n + 1);
+                    }
+                    ok = ok && warp_wait(bar(A_DS_FULL), n & 1, abort_flag, p.err, lim);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(n + 1);
+                    issue_dk(n);
                 }
-                ok = ok && warp_wait(bar(A_P_FULL), n & 1, abort_flag, p.err, lim);
-                if (!ok) break;
-                tc_fence_after();
-                issue_dv(n);
-                ok = ok && warp_wait(bar(A_DS_FULL), n & 1, abort_flag, p.err, lim);
-                if (!ok) break;
-                tc_fence_after();
-                issue_dk(n);
-                if (n + 1 < n_steps) {
-                    // dP^T_{n+1} overwrites dS^T_n: dK has read it.
-                    ok = ok && warp_wait(bar(A_DS_EMPTY), n & 1, abort_flag, p.err, lim);
-                    wait_do(n + 1);
+            } else {
+                const uint64_t dv_a = sdesc_sw128(sbase + L::kV, 16, 1024);
+                const uint64_t dp_a = sdesc_sw128(sbase + L::kP, 16, 1024);
+                const uint64_t do_k = sdesc_sw128(sbase + L::kDR, 16, 1024);
+                const uint64_t do_mn = sdesc_sw128(sbase + L::kDR, kPanelBytes, 1024);
+                auto wait_do = [&](int n) {
+                    ok = ok && warp_wait(bar(A_DO_FULL + n % kSlots), (n / kSlots) & 1, abort_flag, p.err, lim);
+                };
+                // dP^T_n = V dO_n^T
+                auto issue_dp = [&](int n) {
+                    const uint64_t b0 = do_k + slot_off(n);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss(t_dp, dv_a + kmajor_step(kk), b0 + kmajor_step(kk), kIdescT, kk > 0 ? 1u : 0u);
+                        tc_commit(bar(A_DP_FULL));
+                    }
+                    __syncwarp();
+                };
+                // dV += P^T_n dO_n (dO_n as N = d x K = 128 queries, MN-major)
+                auto issue_dv = [&](int n) {
+                    const uint64_t b0 = do_mn + slot_off(n);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < 128 / 16; ++kk)
+                            mma_ss(t_dv, dp_a + kmajor_step(kk), b0 + ((kk * 16 * 128) >> 4), kIdescG,
+                                   (n > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bar(A_P_EMPTY));
+                        tc_commit(bar(A_DO_EMPTY + n % kSlots));
+                        if (n == n_steps - 1) tc_commit(bar(A_DONE + 1));
+                    }
+                    __syncwarp();
+                };
+                wait_do(0);
+                if (ok) issue_dp(0);
+                for (int n = 0; ok && n < n_steps; ++n) {
+                    ok = ok && warp_wait(bar(A_P_FULL), n & 1, abort_flag, p.err, lim);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_dp(n + 1);
+                    issue_dv(n);
+                    if (n + 1 < n_steps) {
+                        // dP^T_{n+1} overwrites dS^T_n: dK has read it.
+                        ok = ok && warp_wait(bar(A_DS_EMPTY), n & 1, abort_flag, p.err, lim);
+                        wait_do(n + 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_dp(n + 1);
+                    }
                 }
             }
-            // Every MMA issued has completed before tensor memory is freed.
+            // Every MMA this warp issued has completed before tensor memory is freed.
             if (elect_one()) {
-                tc_commit(bar(A_DRAIN));
-                mbar_wait_drain(bar(A_DRAIN), 0, lim);
+                tc_commit(bar(A_DRAIN + who));
+                mbar_wait_drain(bar(A_DRAIN + who), 0, lim);
             }
             __syncwarp();
         }
@@ -552,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(A_DS_FULL));
     }
     // ---- epilogue: dV and scale dK -> bf16, this thread's d / 2 columns of its key row
-    if (ok) ok = warp_wait(bar(A_DONE), 0, abort_flag, p.err, lim);
+    if (ok) ok = warp_wait(bar(A_DONE), 0, abort_flag, p.err, lim) && warp_wait(bar(A_DONE + 1), 0, abort_flag, p.err, lim);
     if (ok) {
         tc_fence_after();
         const bool store = r < rows_here;
@@ -626,8 +635,8 @@ enum DqBar : uint32_t {
     B_DS_FULL = 21,   // dS_j in TMEM (8 arrivals)
     B_DQ_DONE = 22,   // dQ += dS_j K_j done
     B_DQ_FINAL = 23,
-    B_DRAIN = 24,
-    B_COUNT = 25,
+    B_DRAIN = 24,     // + issuer (2)
+    B_COUNT = 26,
 };
 
 template <int D, bool CAUSAL>
@@ -739,8 +748,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
-        } else if (warp == 1) {
-            // ================= MMA issuer =================
+        } else {
+            // ================= MMA issuers: warp 1 S and dQ (the K ring),
+            // warp 3 dP (the V ring) =================
+            const int who = warp == 1 ? 0 : 1;
             const uint64_t dq_a = sdesc_sw128(sbase + L::kQ, 16, 1024);
             const uint64_t ddo_a = sdesc_sw128(sbase + L::kDO, 16, 1024);
             const uint64_t dk_b = sdesc_sw128(sbase + L::kKR, 16, 1024);
@@ -795,25 +806,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             };
-            issue_s(0);
-            issue_dp(0);
-            for (int j = 0; ok && j < n_steps; ++j) {
-                if (j + 1 < n_steps) {
-                    // S[(j+1) % 2] held dS_{j-1}: dQ of step j-1 has read it.
-                    if (j >= 1) ok = ok && warp_wait(bar(B_DQ_DONE), (j - 1) & 1, abort_flag, p.err, lim);
-                    issue_s(j + 1);
+            if (who == 0) {
+                issue_s(0);
+                for (int j = 0; ok && j < n_steps; ++j) {
+                    if (j + 1 < n_steps) {
+                        // S[(j+1) % 2] held dS_{j-1}: dQ of step j-1 has read it.
+                        if (j >= 1) ok = ok && warp_wait(bar(B_DQ_DONE), (j - 1) & 1, abort_flag, p.err, lim);
+                        issue_s(j + 1);
+                    }
+                    ok = ok && warp_wait(bar(B_DS_FULL), j & 1, abort_flag, p.err, lim);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_dq(j);
+                }
+            } else {
+                issue_dp(0);
+                for (int j = 0; ok && j + 1 < n_steps; ++j) {
                     // dP_{j+1} overwrites dP_j: the compute warps have read it.
                     ok = ok && warp_wait(bar(B_DP_FREE), j & 1, abort_flag, p.err, lim);
                     issue_dp(j + 1);
                 }
-                ok = ok && warp_wait(bar(B_DS_FULL), j & 1, abort_flag, p.err, lim);
-                if (!ok) break;
-                tc_fence_after();
-                issue_dq(j);
             }
             if (elect_one()) {
-                tc_commit(bar(B_DRAIN));
-                mbar_wait_drain(bar(B_DRAIN), 0, lim);
+                tc_commit(bar(B_DRAIN + who));
+                mbar_wait_drain(bar(B_DRAIN + who), 0, lim);
             }
             __syncwarp();
         }
