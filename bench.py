@@ -263,6 +263,7 @@ def ours(args, world, rank, local):
     do_decode = args.case in ("all", "decode")
     do_chunk = args.case in ("all", "chunk")
     do_packed = args.case in ("all", "packed")
+    do_bwd = args.case in ("all", "backward")
     q, k, v = W.dense_inputs(B, N, H, d, SEED_C3, dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -337,6 +338,23 @@ def ours(args, world, rank, local):
         if st != F.FA_OK:
             raise F.FAError(st, "fa_qkvpacked_fwd")
 
+    # backward on the prefill shape: dO drawn once, O and LSE from the forward
+    if do_bwd:
+        dout = W.randn_bf16_device((B, N, H, d), SEED_C3 * 7 + 1, dev)
+        bo_nc, bl_nc = F.attention(q, k, v, scale=scale, causal=False)
+        bo_c, bl_c = F.attention(q, k, v, scale=scale, causal=True)
+        g_q, g_k, g_v = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws_bytes = F.fa_bwd_workspace_bytes(B, B * N, H)
+        bws = torch.empty(bws_bytes, dtype=torch.uint8, device=dev)
+
+    def backward(causal):
+        if not do_bwd:
+            return
+        bo, bl = (bo_c, bl_c) if causal else (bo_nc, bl_nc)
+        st = F.fa_bwd(q, k, v, bo, bl, dout, g_q, g_k, g_v, bws, bws_bytes, B, H, H, N, d, scale, causal, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_bwd")
+
     def store():
         if not do_chunk:
             return
@@ -371,6 +389,8 @@ def ours(args, world, rank, local):
         chunk()
         chunk_contiguous()
         packed()
+        backward(False)
+        backward(True)
     torch.cuda.synchronize()
     st = F.fa_device_status(sp)
     if st != F.FA_OK:
@@ -405,7 +425,7 @@ def ours(args, world, rank, local):
     # the main one, so that their power draw does not change the clocks the
     # main legs run at.
     K2 = min(K, 100)
-    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K2)]
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K2)]
     for s in range(K2):
         flush.zero_()
         e = ev2[s]
@@ -418,6 +438,17 @@ def ours(args, world, rank, local):
         e[3].record(stream)
         packed()
         e[4].record(stream)
+        flush.zero_()
+        e[5].record(stream)
+        backward(False)
+        e[6].record(stream)
+    # the causal backward in its own pass (the flush sits between the legs)
+    ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K2)]
+    for s in range(K2):
+        flush.zero_()
+        ev3[s][0].record(stream)
+        backward(True)
+        ev3[s][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     st = F.fa_device_status(sp)
@@ -432,8 +463,10 @@ def ours(args, world, rank, local):
     t_chunk = sum(e[1].elapsed_time(e[2]) for e in ev2) / K2
     t_chunk_c = sum(e[2].elapsed_time(e[3]) for e in ev2) / K2
     t_packed = sum(e[3].elapsed_time(e[4]) for e in ev2) / K2
-    t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed = (
-        max_over_ranks(world, x) for x in (t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed))
+    t_bnc = sum(e[5].elapsed_time(e[6]) for e in ev2) / K2
+    t_bc = sum(e[0].elapsed_time(e[1]) for e in ev3) / K2
+    t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed, t_bnc, t_bc = (
+        max_over_ranks(world, x) for x in (t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed, t_bnc, t_bc))
     # continuation FLOPs, causal bottom-right, halved-square convention of
     # the varlen leg: 4 d H (Lq (Lk - Lq) + Lq^2 / 2) per sequence
     f_chunk = sum(4.0 * cd * cH * (lq_ * (lk_ - lq_) + lq_ * lq_ / 2) for lq_, lk_ in zip(cl_q, cl_k))
@@ -457,7 +490,11 @@ def ours(args, world, rank, local):
                               "chunk_tflops": f_chunk / (t_chunk * 1e-3) / 1e12 if do_chunk else None,
                               "chunk_contiguous_tflops": f_chunk / (t_chunk_c * 1e-3) / 1e12 if do_chunk else None,
                               "store_gbs": store_bytes / (t_store * 1e-3) / 1e9 if do_chunk else None,
-                              "qkvpacked_ms": t_packed}), flush=True)
+                              "qkvpacked_ms": t_packed,
+                              "backward_ms": [t_bnc, t_bc],
+                              "backward_tflops": [2.5 * f_nc / (t_bnc * 1e-3) / 1e12,
+                                                  2.5 * f_c / (t_bc * 1e-3) / 1e12] if do_bwd else None}),
+              flush=True)
         return
 
     # ---- end to end through the public API with pinned host buffers.  Each
@@ -550,6 +587,14 @@ def ours(args, world, rank, local):
             "same_chunk_contiguous_kv": {"ms": t_chunk_c, "tflops": f_chunk / (t_chunk_c * 1e-3) / 1e12},
             "qkvpacked_noncausal": {"ms": t_packed, "tflops": f_nc / (t_packed * 1e-3) / 1e12,
                                     "frac_bf16_peak": f_nc / (t_packed * 1e-3) / 1e12 / peak_tf},
+            # backward FLOPs by the usual count of 5 products (2.5x the
+            # forward's); the kernels execute 7 (S and dP in both kernels)
+            "backward_noncausal": {"ms": t_bnc, "tflops": 2.5 * f_nc / (t_bnc * 1e-3) / 1e12,
+                                   "tflops_executed": 3.5 * f_nc / (t_bnc * 1e-3) / 1e12,
+                                   "frac_bf16_peak_executed": 3.5 * f_nc / (t_bnc * 1e-3) / 1e12 / peak_tf},
+            "backward_causal": {"ms": t_bc, "tflops": 2.5 * f_c / (t_bc * 1e-3) / 1e12,
+                                "tflops_executed": 3.5 * f_c / (t_bc * 1e-3) / 1e12,
+                                "frac_bf16_peak_executed": 3.5 * f_c / (t_bc * 1e-3) / 1e12 / peak_tf},
         },
         "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": tflops / peak_tf, "traffic": PREFILL_TRAFFIC_BYTES,
@@ -560,9 +605,10 @@ def ours(args, world, rank, local):
         "e2e": {"value": e2e_tflops * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "prefill legs with q,k,v copied from pinned host memory and O, LSE copied back each step; "
                         "steps double-buffered over copy-in, compute and copy-out streams"},
-        "gpu_launches": 5 * K + 4 * K2,
-        "follow_up_legs": f"store_kvcache, paged_prefill_chunk, same_chunk_contiguous_kv and qkvpacked_noncausal: "
-                          f"{K2} steps of their own after the main timed loop, not in ms_per_step or value",
+        "gpu_launches": 5 * K + 4 * K2 + 6 * K2,
+        "follow_up_legs": f"store_kvcache, paged_prefill_chunk, same_chunk_contiguous_kv, qkvpacked_noncausal and "
+                          f"backward_(non)causal: {K2} steps of their own after the main timed loop, not in "
+                          f"ms_per_step or value",
         "clocks": clk,
         "wall_s_timed": wall,
     }
@@ -579,7 +625,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode", "chunk", "packed"], default="all",
+    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode", "chunk", "packed", "backward"],
+                    default="all",
                     help="run only one leg (for profiling); prints a short line instead of the bench line")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences of the decode leg (profiling)")
     ap.add_argument("--decode-hkv", type=int, default=32,
