@@ -824,6 +824,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; ok && j + 1 < n_steps; ++j) {
                     // dP_{j+1} overwrites dP_j: the compute warps have read it.
                     ok = ok && warp_wait(bar(B_DP_FREE), j & 1, abort_flag, p.err, lim);
+                    // S_{j+1} goes through the tensor pipe first: the compute
+                    // warps need it first, dP_{j+1} only after their exponentials.
+                    ok = ok && warp_wait(bar(B_S_FULL + ((j + 1) & 1)), ((j + 1) >> 1) & 1, abort_flag, p.err, lim);
                     issue_dp(j + 1);
                 }
             }
