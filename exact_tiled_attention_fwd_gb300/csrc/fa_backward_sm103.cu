@@ -279,7 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t lim = p.wait_limit_ns;
     // step n -> (query head, query block)
     auto step_head = [&](int n) { return hk * p.group + n / per_head; };
-    auto step_block = [&](int n) { return i_lo + n % per_head; };
+    // Each CTA starts its walk over the query blocks at its own offset (its
+    // key block index), so that the CTAs of one head, which run at the same
+    // time, ask for different Q / dO tiles at any moment: a tile is fetched
+    // from memory once and then read from L2 by the others.
+    const int rot = per_head > 0 ? jb % per_head : 0;
+    auto step_block = [&](int n) {
+        const int m = n % per_head + rot;
+        return i_lo + (m >= per_head ? m - per_head : m);
+    };
 
     // 128 * 72 + 256 * 216 = 64,512 = 384 * 168 (the launch's registers).
     constexpr uint32_t kRegsLow = 72, kRegsHigh = 216;
@@ -676,6 +684,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_steps = max_key < 0 ? 0 : min(n_steps, max_key / kBlockN + 1);
     }
     const int rows_here = r_last - row0 + 1;
+    // Step j reads key block kblock(j): each CTA starts its walk at its own
+    // offset, so the CTAs of a head ask for different K / V tiles at once.
+    const int rot = n_steps > 0 ? ib % n_steps : 0;
+    auto kblock = [&](int j) {
+        const int m = j + rot;
+        return m >= n_steps ? m - n_steps : m;
+    };
     if (n_steps == 0) {
         // No row of the block sees a key: dQ = 0.
         for (int e = threadIdx.x; e < rows_here * (D / 8); e += kThreads) {
@@ -738,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int pn = 0; pn < kPanels; ++pn)
                         tma_load_3d(sbase + ring + sl * L::kTile + pn * kPanelBytes, map, bar(full + sl), pn * 64, hk,
-                                    g.k_start + j * kBlockN);
+                                    g.k_start + kblock(j) * kBlockN);
                 }
                 // Drain: the last fill of every slot (and Q / dO).
                 if (is_k) mbar_wait_drain(bar(B_QD_FULL), 0, lim);
@@ -870,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld64(t_row + c_s, u);
         // keys past the sequence, and (causal) keys past row + diag, get P = 0
         // (only blocks that reach past the sequence end or the diagonal)
-        const int kbase = j * kBlockN + 64 * half;
+        const int kbase = kblock(j) * kBlockN + 64 * half;
         int lim_c = g.Lk - 1 - kbase;
         if (CAUSAL) lim_c = min(lim_c, row + diag - kbase);
         const bool masked = __any_sync(0xffffffffu, lim_c < 63);
