@@ -666,11 +666,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Grid as the forward's: causal (head, block from the last, sequence) so
-    // the blocks with the most keys go first; otherwise (block, head, sequence).
+    // Grid (block, head, sequence), blocks fastest, so the CTAs resident at
+    // once cover few heads and their K/V stay in L2; with causal masking the
+    // blocks run from the last (most keys) to the first within each head.
+    // (Heaviest first across all heads, as the causal forward does, kept
+    // every head's K/V live at once and missed L2 on 3.5x the algorithmic
+    // bytes; this order measured 3% faster at B1 H32 N8192 d128.)
     const int seq = blockIdx.z;
-    const int h = CAUSAL ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
-    const int ib = CAUSAL ? (p.num_q_blocks - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.x);
+    const int h = static_cast<int>(blockIdx.y);
+    const int ib = CAUSAL ? (p.num_q_blocks - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
     const int hk = h / p.group;
     Geom g;
     if (!seq_geom(p, seq, ib == 0 && h == 0 && threadIdx.x == 0, g)) return;
@@ -971,7 +975,7 @@ cudaError_t launch_dc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     auto kb = bwd_dq_kernel<D, CAUSAL>;
     e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(DqSmem<D>::kDyn));
     if (e != cudaSuccess) return e;
-    const dim3 gb = CAUSAL ? dim3(p.H, p.num_q_blocks, p.num_seqs) : dim3(p.num_q_blocks, p.H, p.num_seqs);
+    const dim3 gb(p.num_q_blocks, p.H, p.num_seqs);
     kb<<<gb, kThreads, DqSmem<D>::kDyn, stream>>>(tq, tk, tv, tdo, p);
     return cudaGetLastError();
 }

@@ -144,9 +144,49 @@ __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(con
         for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
     }
 
-    for (int pg = t0 / kPageSize; pg * kPageSize < t1; ++pg) {
-        const int page = lookup_page(p.block_table, p.max_pages, p.num_pages, b, pg, p.err);
-        if (page < 0) continue;
+    // The page walk runs ahead of the loads: the K/V rows of the page kAhead
+    // pages on are pulled into L2 while this page is computed, and table
+    // entries are fetched one page before that, so a page's loads find their
+    // lines in L2 instead of waiting on a dependent table load and then on
+    // HBM.  Grouped warps, which compute longer per page, look two pages ahead
+    // (measured 4.5% faster with 4 heads per warp, no gain for one).
+    const int pg0 = t0 / kPageSize;
+    const int pg_end = (t1 + kPageSize - 1) / kPageSize;
+    auto entry = [&](int pg) {
+        return pg < pg_end ? lookup_page(p.block_table, p.max_pages, p.num_pages, b, pg, p.err) : -1;
+    };
+    // L2 prefetch of one page of this warp's kv head: lane l takes the
+    // 128-byte lines l * kPf .. l * kPf + kPf - 1 of the page's K lines
+    // followed by its V lines (row = line / kLinesPerRow).
+    constexpr int kLinesPerRow = D / 64;
+    constexpr int kLinesPerPage = kPageSize * kLinesPerRow;  // per tensor
+    constexpr int kPf = 2 * kLinesPerPage / 32;              // prefetches per lane
+    static_assert(kPf * 32 == 2 * kLinesPerPage, "page lines per lane");
+    auto prefetch_page = [&](int page) {
+        if (page < 0) return;
+#pragma unroll
+        for (int x = 0; x < kPf; ++x) {
+            const int line = lane * kPf + x;
+            const int tl = line % kLinesPerPage;
+            const uint16_t* a = (line < kLinesPerPage ? kc : vc) +
+                                paged_row_offset(page, tl / kLinesPerRow, p.Hkv, hk, D) + (tl % kLinesPerRow) * 64;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        }
+    };
+    constexpr int kAhead = G == 1 ? 1 : 2;
+    int ent[kAhead + 1];  // table entries of pages pg .. pg + kAhead
+#pragma unroll
+    for (int a = 0; a <= kAhead; ++a) ent[a] = entry(pg0 + a);
+#pragma unroll
+    for (int a = 1; a < kAhead; ++a) prefetch_page(ent[a]);
+    for (int pg = pg0; pg < pg_end; ++pg) {
+        const int page = ent[0];
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) ent[a] = ent[a + 1];
+        if (page < 0) {  // outside the pool: skipped (and reported by entry())
+            ent[kAhead] = entry(pg + kAhead + 1);
+            continue;
+        }
         uint4 kv[NI], vv[NI];
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
@@ -158,6 +198,8 @@ __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(con
             const size_t off = paged_row_offset(page, i * RPI + g, p.Hkv, hk, D) + c * 8;
             vv[i] = ldg_stream(vc + off);
         }
+        prefetch_page(ent[kAhead - 1]);
+        ent[kAhead] = entry(pg + kAhead + 1);
 #pragma unroll
         for (int j = 0; j < G; ++j) {
             float s[NI];

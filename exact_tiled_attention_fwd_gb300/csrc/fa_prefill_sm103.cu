@@ -314,6 +314,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j + 1 < nmax) load(pos_k(j + 1), true, j + 1);
                         load(pos_v(j, nmax), false, j);
                     }
+                    // Every load of this CTA is issued: pull into L2 the Q tiles
+                    // of the CTA one wave of SMs further in the grid, which is
+                    // about the one that takes an SM when this CTA ends.
+                    if (p.cu_q == nullptr) {
+                        uint32_t nsm;
+                        asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+                        const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                                               (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z) +
+                                              nsm;
+                        if (lin < static_cast<long long>(gridDim.x) * gridDim.y * gridDim.z) {
+                            const int bx = static_cast<int>(lin % gridDim.x);
+                            const long long r2 = lin / gridDim.x;
+                            const int by = static_cast<int>(r2 % gridDim.y);
+                            const int bz = static_cast<int>(r2 / gridDim.y);
+                            const int h2 = CAUSAL ? bx : by;
+                            const int qb2 = CAUSAL ? (nblk - 1 - by) : bx;
+#pragma unroll
+                            for (int t = 0; t < kTiles; ++t) {
+                                const int rr = qb2 * kBlockM * kTiles + t * kBlockM;
+                                if (rr >= p.N) continue;
+#pragma unroll
+                                for (int pn = 0; pn < kPanels; ++pn)
+                                    asm volatile(
+                                        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                                            reinterpret_cast<uint64_t>(&tm_q)),
+                                        "r"(pn * 64), "r"(h2), "r"(bz * p.N + rr)
+                                        : "memory");
+                            }
+                        }
+                    }
                 }
             } else {
                 // Paged K/V: the whole warp runs the loop (its waits are
