@@ -200,43 +200,143 @@ __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(con
         }
         prefetch_page(ent[kAhead - 1]);
         ent[kAhead] = entry(pg + kAhead + 1);
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-            float s[NI];
-#pragma unroll
-            for (int i = 0; i < NI; ++i) s[i] = dot8(qf[j], kv[i]);
-#pragma unroll
-            for (int off = LPR / 2; off >= 1; off >>= 1) {
-#pragma unroll
-                for (int i = 0; i < NI; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
+        if constexpr (G == 1) {
+    #pragma unroll
+            for (int j = 0; j < G; ++j) {
+                float s[NI];
+    #pragma unroll
+                for (int i = 0; i < NI; ++i) s[i] = dot8(qf[j], kv[i]);
+    #pragma unroll
+                for (int off = LPR / 2; off >= 1; off >>= 1) {
+    #pragma unroll
+                    for (int i = 0; i < NI; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
+                }
+                float mp = neg_inf();
+    #pragma unroll
+                for (int i = 0; i < NI; ++i) {
+                    const int tok = pg * kPageSize + i * RPI + g;
+                    if (tok >= t1) s[i] = neg_inf();
+                    mp = fmaxf(mp, s[i]);
+                }
+    #pragma unroll
+                for (int off = LPR; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, off));
+                const float m_new = fmaxf(m[j], mp);
+                const float mu = m_new == neg_inf() ? 0.f : m_new;
+                const float alpha = ex2(m[j] - mu);  // m = -inf -> 0
+                l[j] *= alpha;
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) acc[j][e] *= alpha;
+    #pragma unroll
+                for (int i = 0; i < NI; ++i) {
+                    const float pi = ex2(s[i] - mu);
+                    l[j] += pi;
+                    axpy8(acc[j], pi, vv[i]);
+                }
+                m[j] = m_new;
             }
-            float mp = neg_inf();
+        } else {
+            // Grouped heads.  Each K/V chunk is unpacked to fp32 pairs once and
+            // used by all G heads with packed fp32x2 arithmetic.  The row sums
+            // of the partial dot products are reduced by halving: at each xor
+            // level a lane keeps half of its values (the upper half if its
+            // lane bit is set) and adds the partner's matching half, so after
+            // log2(LPR) levels lane c of a row group holds the whole score of
+            // row c / 2 of its group (lanes c and c ^ 1 hold the same row).
+            float sc[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                float sv[NI];
+#pragma unroll
+                for (int i = 0; i < NI; ++i) {
+                    const float2 k0 = make_float2(bf16lo_to_f32(kv[i].x), bf16hi_to_f32(kv[i].x));
+                    const float2 k1 = make_float2(bf16lo_to_f32(kv[i].y), bf16hi_to_f32(kv[i].y));
+                    const float2 k2 = make_float2(bf16lo_to_f32(kv[i].z), bf16hi_to_f32(kv[i].z));
+                    const float2 k3 = make_float2(bf16lo_to_f32(kv[i].w), bf16hi_to_f32(kv[i].w));
+                    float2 a = __fmul2_rn(make_float2(qf[j][0], qf[j][1]), k0);
+                    a = __ffma2_rn(make_float2(qf[j][2], qf[j][3]), k1, a);
+                    a = __ffma2_rn(make_float2(qf[j][4], qf[j][5]), k2, a);
+                    a = __ffma2_rn(make_float2(qf[j][6], qf[j][7]), k3, a);
+                    sv[i] = a.x + a.y;
+                }
+                int n = NI;
+#pragma unroll
+                for (int off = LPR / 2; off >= 1; off >>= 1) {
+                    if (n > 1) {
+                        const bool up = (c & off) != 0;
+                        n >>= 1;
+#pragma unroll
+                        for (int k = 0; k < NI / 2; ++k) {
+                            if (k < n) {
+                                const float keep = up ? sv[k + n] : sv[k];
+                                const float send = up ? sv[k] : sv[k + n];
+                                sv[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                            }
+                        }
+                    } else {
+                        sv[0] += __shfl_xor_sync(0xffffffffu, sv[0], off);
+                    }
+                }
+                const int tok = pg * kPageSize + (c >> 1) * RPI + g;
+                sc[j] = tok < t1 ? sv[0] : neg_inf();
+            }
+            // Page maximum (lane pairs hold equal rows, so xor 1 is skipped),
+            // then each lane's own row probability.
+            float pl[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                float mp = sc[j];
+#pragma unroll
+                for (int off = 2; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, off));
+                const float m_new = fmaxf(m[j], mp);
+                const float mu = m_new == neg_inf() ? 0.f : m_new;
+                const float alpha = ex2(m[j] - mu);  // m = -inf -> 0
+                pl[j] = ex2(sc[j] - mu);
+                l[j] = l[j] * alpha + ((c & 1) == 0 ? pl[j] : 0.f);  // each row once
+                const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 o = __fmul2_rn(make_float2(acc[j][e], acc[j][e + 1]), a2);
+                    acc[j][e] = o.x;
+                    acc[j][e + 1] = o.y;
+                }
+                m[j] = m_new;
+            }
+            // O += p V: row i of this lane's group is held by lane g * LPR + 2 i.
 #pragma unroll
             for (int i = 0; i < NI; ++i) {
-                const int tok = pg * kPageSize + i * RPI + g;
-                if (tok >= t1) s[i] = neg_inf();
-                mp = fmaxf(mp, s[i]);
+                const float2 v0 = make_float2(bf16lo_to_f32(vv[i].x), bf16hi_to_f32(vv[i].x));
+                const float2 v1 = make_float2(bf16lo_to_f32(vv[i].y), bf16hi_to_f32(vv[i].y));
+                const float2 v2 = make_float2(bf16lo_to_f32(vv[i].z), bf16hi_to_f32(vv[i].z));
+                const float2 v3 = make_float2(bf16lo_to_f32(vv[i].w), bf16hi_to_f32(vv[i].w));
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const float pi = __shfl_sync(0xffffffffu, pl[j], g * LPR + 2 * i);
+                    const float2 p2 = make_float2(pi, pi);
+                    float2 o = __ffma2_rn(p2, v0, make_float2(acc[j][0], acc[j][1]));
+                    acc[j][0] = o.x;
+                    acc[j][1] = o.y;
+                    o = __ffma2_rn(p2, v1, make_float2(acc[j][2], acc[j][3]));
+                    acc[j][2] = o.x;
+                    acc[j][3] = o.y;
+                    o = __ffma2_rn(p2, v2, make_float2(acc[j][4], acc[j][5]));
+                    acc[j][4] = o.x;
+                    acc[j][5] = o.y;
+                    o = __ffma2_rn(p2, v3, make_float2(acc[j][6], acc[j][7]));
+                    acc[j][6] = o.x;
+                    acc[j][7] = o.y;
+                }
             }
-#pragma unroll
-            for (int off = LPR; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, off));
-            const float m_new = fmaxf(m[j], mp);
-            const float mu = m_new == neg_inf() ? 0.f : m_new;
-            const float alpha = ex2(m[j] - mu);  // m = -inf -> 0
-            l[j] *= alpha;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[j][e] *= alpha;
-#pragma unroll
-            for (int i = 0; i < NI; ++i) {
-                const float pi = ex2(s[i] - mu);
-                l[j] += pi;
-                axpy8(acc[j], pi, vv[i]);
-            }
-            m[j] = m_new;
         }
     }
-    // Sum the row groups: every lane of a group holds the same l; chunks add.
+    // Sum the row groups: chunks add.  With G = 1 every lane of a group holds
+    // the group's l; with grouped heads each even lane holds its own row's
+    // share, so l is summed over every lane.
 #pragma unroll
     for (int j = 0; j < G; ++j) {
+        if (G > 1) {
+#pragma unroll
+            for (int off = 1; off < LPR; off <<= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
+        }
 #pragma unroll
         for (int off = LPR; off < 32; off <<= 1) {
             l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
