@@ -543,6 +543,10 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
     if (workspace_bytes < fa_bwd_workspace_bytes(num_seqs, total_q, H)) return FA_ERR_INVALID;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
+    // grid.x of the two main kernels enumerates (128-row block, head) pairs
+    if (static_cast<long long>((max_seqlen_q + fa::kBlockM - 1) / fa::kBlockM) * H > 2147483647ll ||
+        static_cast<long long>((max_seqlen_k + fa::kBlockN - 1) / fa::kBlockN) * Hkv > 2147483647ll)
+        return FA_ERR_UNSUPPORTED;
     unsigned int* err = nullptr;
     fa_status st = ensure_init(&err);
     if (st != FA_OK) return st;
