@@ -160,6 +160,8 @@ fa_status dense_impl(Operand q, Operand k, Operand v, void* o, float* lse, int B
     p.err = err;
     p.wait_limit_ns = wait_limit_ns();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the causal grid enumerates (256-row block, head) pairs in grid.x
+    if (static_cast<long long>((p.num_q_blocks + 1) / 2) * H > 2147483647ll) return FA_ERR_UNSUPPORTED;
     return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
 }
 
@@ -203,6 +205,8 @@ fa_status varlen_impl(Operand q, Operand k, Operand v, void* o, float* lse, cons
     p.err = err;
     p.wait_limit_ns = wait_limit_ns();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the causal grid enumerates (256-row block, head) pairs in grid.x
+    if (static_cast<long long>((p.num_q_blocks + 1) / 2) * H > 2147483647ll) return FA_ERR_UNSUPPORTED;
     return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
 }
 
@@ -311,6 +315,8 @@ int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the causal grid enumerates (256-row block, head) pairs in grid.x
+    if (static_cast<long long>((p.num_q_blocks + 1) / 2) * H > 2147483647ll) return FA_ERR_UNSUPPORTED;
     return finish(fa::launch_prefill(tq, tk, tv, p, d, causal != 0, s), s);
 }
 
