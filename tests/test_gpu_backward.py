@@ -95,7 +95,8 @@ def run_dense(fa, B, N, H, Hkv, d, causal, seed):
 
 
 @pytest.mark.parametrize("B,N,H,Hkv,d", [(2, 300, 4, 4, 128), (1, 517, 4, 2, 64), (3, 128, 2, 1, 128),
-                                         (1, 1, 2, 2, 64), (1, 700, 2, 2, 128), (2, 257, 6, 3, 64)])
+                                         (1, 1, 2, 2, 64), (1, 700, 2, 2, 128), (2, 257, 6, 3, 64),
+                                         (2, 300, 12, 12, 128), (1, 400, 12, 4, 64)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_dense_backward(fa, B, N, H, Hkv, d, causal):
     (q, k, v, do, scale), got = run_dense(fa, B, N, H, Hkv, d, causal, seed=60 + N + d)

@@ -86,6 +86,13 @@ def test_gqa(fa, H, Hkv):
     check_full(fa, 1, 200, H, 64, False, seed=56, Hkv=Hkv)
 
 
+def test_head_groups(fa):
+    """Causal d = 128 hands out (block, head) pairs in groups of 8 heads:
+    12 heads make one full group and one of 4, over two batches."""
+    check_full(fa, 2, 700, 12, 128, True, seed=58)
+    check_full(fa, 2, 700, 12, 128, True, seed=59, Hkv=4)
+
+
 def test_triton_tutorial_shape(fa):
     """The [2, 4, 1024, 64] case the yulong.wang page checks its kernel on."""
     check_full(fa, 2, 1024, 4, 64, False, seed=0)
