@@ -381,6 +381,65 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
     unsigned int* err = nullptr;
     fa_status st = ensure_init(&err);
     if (st != FA_OK) return st;
+    const int group = H / Hkv;
+    if (group >= fa::kDecodeTcMinGroup && group <= 2 * fa::kBlockM && static_cast<long long>(B) * Hkv <= 65535 &&
+        (static_cast<long long>(num_pages) + 1) * page_size <= (1ll << 31) - 1) {
+        // Large query groups: the tensor-core decode (the group's query heads
+        // are the rows of a Q tile), then the combine step.
+        const long long pool_rows = static_cast<long long>(num_pages) * page_size;
+        CUtensorMap tq, tk, tv;
+        if ((st = make_map(&tq, q, d, 1, static_cast<long long>(B) * H)) != FA_OK) return st;
+        if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, fa::kPageSize)) != FA_OK) return st;
+        if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, fa::kPageSize)) != FA_OK) return st;
+        const int T = fa::kDecodeTcSplitTokens;
+        const int splits = max_seqlen > T ? (max_seqlen + T - 1) / T : 1;
+        const size_t slots = static_cast<size_t>(B) * H * splits;
+        float* ws_o = static_cast<float*>(workspace);
+        float* ws_ml =
+            reinterpret_cast<float*>(static_cast<char*>(workspace) + ((slots * d * sizeof(float) + 255) & ~size_t(255)));
+        fa::PrefillParams pp{};
+        pp.num_seqs = B * Hkv;
+        pp.H = 1;
+        pp.Hkv = Hkv;
+        pp.group = 1;
+        pp.max_seqlen_q = group;
+        pp.max_seqlen_k = max_seqlen;
+        pp.total_q = B * H;
+        pp.num_q_blocks = (group + fa::kBlockM - 1) / fa::kBlockM;
+        pp.scale_log2 = scale * 1.4426950408889634f;
+        pp.err = err;
+        pp.wait_limit_ns = wait_limit_ns();
+        pp.block_table = block_table;
+        pp.max_pages = max_pages_per_seq;
+        pp.num_pages = num_pages;
+        pp.seqlens = seqlens;
+        pp.decode_group = group;
+        pp.split_tokens = T;
+        pp.max_splits = splits;
+        pp.ws_o = ws_o;
+        pp.ws_ml = ws_ml;
+        fa::DecodeParams p{};
+        p.seqlens = seqlens;
+        p.o = o;
+        p.lse = lse;
+        p.B = B;
+        p.H = H;
+        p.Hkv = Hkv;
+        p.group = group;
+        p.num_pages = num_pages;
+        p.max_pages = max_pages_per_seq;
+        p.max_seqlen = max_seqlen;
+        p.split_tokens = T;
+        p.max_splits = splits;
+        p.ws_o = ws_o;
+        p.ws_ml = ws_ml;
+        p.scale_log2 = pp.scale_log2;
+        p.err = err;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        cudaError_t e = fa::launch_prefill(tq, tk, tv, pp, d, false, s);
+        if (e == cudaSuccess) e = fa::launch_decode_combine(p, d, s);
+        return finish(e, s);
+    }
     fa::DecodeParams p{};
     p.q = q;
     p.k_cache = k_cache;

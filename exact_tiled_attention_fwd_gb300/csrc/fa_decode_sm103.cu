@@ -500,6 +500,15 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t stream) {
+    dim3 cgrid((p.B * p.H + kDecodeWarps - 1) / kDecodeWarps);
+    if (d == 128)
+        decode_combine_kernel<128><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
+    else
+        decode_combine_kernel<64><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
     dim3 grid((p.max_seqlen + kPageSize - 1) / kPageSize, p.B);
     gather_kernel<<<grid, 256, 0, stream>>>(p);

@@ -42,6 +42,17 @@ struct PrefillParams {
     // kPageSize-row boxes.
     const int* block_table;
     int max_pages, num_pages;
+    // Grouped decode on the tensor cores (decode_group > 0, with a page
+    // table): CTA (split, 0, s) takes the decode_group query heads of pair
+    // s = (b, kv head) = (s / Hkv, s % Hkv) as its query rows (q viewed as
+    // [B * H, 1, d]) and the keys [split * split_tokens, ...) of sequence b
+    // (seqlens[b] keys), and writes the split's unnormalised O and (m, l) to
+    // ws_o / ws_ml at slot (b * H + head) * max_splits + split, the layout of
+    // DecodeParams below; the combine kernel then merges the splits.
+    const int* seqlens;
+    int decode_group, split_tokens, max_splits;
+    float* ws_o;
+    float* ws_ml;
 };
 
 struct DecodeParams {
@@ -76,6 +87,8 @@ struct GatherParams {
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int d, bool causal, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
+// The combine step alone (after a split kernel that filled ws_o / ws_ml).
+cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream);
 
@@ -140,6 +153,11 @@ cudaError_t static_scratch(void** ptr, size_t* bytes);
 
 // Decode split sizing shared by the workspace query and the launch.
 inline int decode_split_tokens(int /*max_seqlen*/) { return 512; }
+// Query groups of at least this many heads per kv head decode on the tensor
+// cores, in splits of kDecodeTcSplitTokens keys (a multiple of the 512 above,
+// so the partials fit the same workspace).
+constexpr int kDecodeTcMinGroup = 8;
+constexpr int kDecodeTcSplitTokens = 2048;
 inline int decode_max_splits(int max_seqlen) {
     const int t = decode_split_tokens(max_seqlen);
     const int s = (max_seqlen + t - 1) / t;

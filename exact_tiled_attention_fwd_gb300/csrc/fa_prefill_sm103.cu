@@ -173,7 +173,7 @@ __device__ __forceinline__ void cta_unit(int x, int y, int nblk, int nheads, int
     h = grp * hg + rem % gs;
 }
 
-template <int D, bool CAUSAL, bool PAGED>
+template <int D, bool CAUSAL, bool PAGED, bool DECODE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -191,16 +191,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Dispatch order: cta_unit above; grid.z is the sequence.
+    // Dispatch order: cta_unit above; grid.z is the sequence (with DECODE the
+    // (sequence, kv head) pair, and grid.x the split of its keys).
     const int seq = blockIdx.z;
     const int nblk = (p.num_q_blocks + 1) / 2;  // 256-row blocks
-    int qb, h;
-    cta_unit<D, CAUSAL>(static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y), nblk, p.H, qb, h);
-    const int hk = h / p.group;
+    int qb = 0, h = 0;
+    if (!DECODE) cta_unit<D, CAUSAL>(static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y), nblk, p.H, qb, h);
+    const int hk = DECODE ? seq % p.Hkv : h / p.group;
 
     // ---- sequence geometry (uniform over the CTA)
     int q_start, Lq, k_start, Lk;
-    if (p.cu_q != nullptr) {
+    const int* bt_row = PAGED ? p.block_table + static_cast<size_t>(seq) * p.max_pages : nullptr;
+    const int split = DECODE ? static_cast<int>(blockIdx.x) : 0;
+    if (DECODE) {
+        // The decode_group query heads of kv head hk of sequence b are the
+        // query rows; this split's keys are a sub-sequence of b's pages.
+        const int b = seq / p.Hkv;
+        int L = __ldg(p.seqlens + b);
+        if (L < 0 || L > p.max_seqlen_k) {  // clamped as the combine step does
+            if (threadIdx.x == 0 && split == 0 && hk == 0) atomicOr(p.err, FA_DEVERR_INDEX);
+            L = L < 0 ? 0 : p.max_seqlen_k;
+        }
+        const int kbeg = split * p.split_tokens;
+        if (kbeg >= L) return;
+        Lk = min(p.split_tokens, L - kbeg);
+        k_start = 0;
+        q_start = seq * p.decode_group;
+        Lq = p.decode_group;
+        bt_row = p.block_table + static_cast<size_t>(b) * p.max_pages + kbeg / kPageSize;
+    } else if (p.cu_q != nullptr) {
         q_start = p.cu_q[seq];
         Lq = p.cu_q[seq + 1] - q_start;
         k_start = p.cu_k[seq];
@@ -235,8 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long lse_base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
-    // Rows of a tile that sees no key at all: O = 0, LSE = -inf.
-    if (warp >= 4) {
+    // Rows of a tile that sees no key at all: O = 0, LSE = -inf.  (A decode
+    // split always has keys.)
+    if (!DECODE && warp >= 4) {
         const int t = (warp - 4) >> 2;
         const int row = row0 + t * kBlockM + (warp & 3) * 32 + lane;
         if (nb[t] == 0 && row <= r_last[t]) {
@@ -384,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pg = lane / kPanels;  // this lane's page of a block
                 const int pn = lane % kPanels;  // and panel
                 const bool boxes = lane < kPagesPerBlock * kPanels;
-                const int* bt = p.block_table + static_cast<size_t>(seq) * p.max_pages;
+                const int* bt = bt_row;
                 // Table entries are fetched one block ahead of their use: the
                 // entries of blocks j and j + 1 are in flight at once, kept by
                 // block parity.
@@ -686,9 +706,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_P_FULL + t));
         }
-        // ---- epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
+        // ---- epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2; with DECODE
+        // the split's unnormalised O and (m, l) for the combine step.
         if (ok) ok = warp_wait(bar(B_O_FINAL + t), 0, abort_flag, p.err, lim);
-        if (ok) {
+        if (DECODE && ok) {
+            tc_fence_after();
+            const bool store = row <= r_last[t];
+            const size_t slot = (static_cast<size_t>(q_start) + row) * p.max_splits + split;
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t o[32];
+                tmem_ld32(t_row + o_col + ch * 32, o);
+                if (store) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[ch * 8 + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                                      __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+                }
+            }
+            if (store) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(l > 0.f ? m_ref : NEG_INF, l);
+        } else if (ok) {
             tc_fence_after();
             const bool store = row <= r_last[t];
             const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
@@ -719,18 +757,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_sync(kThreads);
 }
 
-template <int D, bool CAUSAL, bool PAGED>
+template <int D, bool CAUSAL, bool PAGED, bool DECODE = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      cudaStream_t stream) {
     using L = PrefillSmem<D>;
     static_assert(L::kDyn <= 232448u, "shared memory budget");
     static_assert(L::kSlots <= kMaxSlots, "K/V ring");
-    auto kern = prefill_kernel<D, CAUSAL, PAGED>;
+    auto kern = prefill_kernel<D, CAUSAL, PAGED, DECODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
     if (e != cudaSuccess) return e;
     const int nblk = (p.num_q_blocks + 1) / 2;
-    const dim3 grid = !CAUSAL ? dim3(nblk, p.H, p.num_seqs)
-                              : (D == 128 ? dim3(nblk * p.H, 1, p.num_seqs) : dim3(p.H, nblk, p.num_seqs));
+    const dim3 grid = DECODE    ? dim3(p.max_splits, 1, p.num_seqs)
+                      : !CAUSAL ? dim3(nblk, p.H, p.num_seqs)
+                                : (D == 128 ? dim3(nblk * p.H, 1, p.num_seqs) : dim3(p.H, nblk, p.num_seqs));
     kern<<<grid, kThreads, L::kDyn, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -746,6 +785,11 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int d, bool causal, cudaStream_t stream) {
     const bool paged = p.block_table != nullptr;
+    if (p.decode_group > 0) {
+        if (!paged || causal) return cudaErrorInvalidValue;
+        return d == 128 ? launch_t<128, false, true, true>(tq, tk, tv, p, stream)
+                        : launch_t<64, false, true, true>(tq, tk, tv, p, stream);
+    }
     if (d == 128)
         return paged ? launch_d<128, true>(tq, tk, tv, p, causal, stream) : launch_d<128, false>(tq, tk, tv, p, causal, stream);
     return paged ? launch_d<64, true>(tq, tk, tv, p, causal, stream) : launch_d<64, false>(tq, tk, tv, p, causal, stream);

@@ -56,6 +56,15 @@ def test_gqa_decode(fa, H, Hkv, d):
     check_full(fa, [700, 33, 1, 1500], H, d, seed=22 + H + Hkv, Hkv=Hkv)
 
 
+@pytest.mark.parametrize("H,Hkv,d", [(32, 4, 128), (32, 2, 64), (32, 1, 128), (128, 1, 64), (160, 1, 128)])
+def test_tensor_core_decode(fa, H, Hkv, d):
+    """Groups of 8 or more query heads decode on the tensor cores (the
+    group's heads are the rows of a Q tile; 160 heads fill two tiles), in
+    2048-key splits merged by the combine step: empty, one-token, page-edge
+    and multi-split lengths."""
+    check_full(fa, [0, 1, 15, 16, 17, 700, 2048, 2049, 4500], H, d, seed=30 + H + Hkv + d, Hkv=Hkv)
+
+
 def test_c5_sampled_heads(fa):
     """The full decode batch (B64, H32, d128, lengths U[512, 16384], random
     page permutation): every sequence, three sampled heads, each checked by
