@@ -355,6 +355,28 @@ def ours(args, world, rank, local):
         if st != F.FA_OK:
             raise F.FAError(st, "fa_bwd")
 
+    # grouped-query decode on the same lengths: 8 kv heads (4 query heads per
+    # kv head, the CUDA-core split kernel) and 2 kv heads (16 per kv head,
+    # the tensor-core decode)
+    do_gqa = args.case == "all"
+    gqa = {}
+    if do_gqa:
+        for hkv_g in (8, 2):
+            pg_ = W.paged_inputs(lens, C5["H"], C5["d"], SEED_C5 + hkv_g, dev, Hkv=hkv_g, pool_on_device=True)
+            gws = F.fa_paged_workspace_size(B5, H5, d5, pg_.max_seqlen)
+            gqa[hkv_g] = (pg_, torch.empty_like(pg_.q), torch.empty((B5, H5), dtype=torch.float32, device=dev),
+                          torch.empty(gws, dtype=torch.uint8, device=dev), gws)
+
+    def decode_gqa(hkv_g):
+        if not do_gqa:
+            return
+        pg_, go, gl, gws_t, gws = gqa[hkv_g]
+        st = F.fa_paged_fwd(pg_.q, pg_.k_cache, pg_.v_cache, pg_.block_table, pg_.seqlens, go, gl, B5, H5, hkv_g,
+                            d5, 16, pg_.num_pages, pg_.block_table.shape[1], pg_.max_seqlen, 1.0 / math.sqrt(d5),
+                            True, gws_t, gws, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_paged_fwd (grouped)")
+
     def store():
         if not do_chunk:
             return
@@ -391,6 +413,8 @@ def ours(args, world, rank, local):
         packed()
         backward(False)
         backward(True)
+        decode_gqa(8)
+        decode_gqa(2)
     torch.cuda.synchronize()
     st = F.fa_device_status(sp)
     if st != F.FA_OK:
@@ -442,13 +466,22 @@ def ours(args, world, rank, local):
         e[5].record(stream)
         backward(False)
         e[6].record(stream)
-    # the causal backward in its own pass (the flush sits between the legs)
-    ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K2)]
+    # the causal backward and the grouped decodes in a pass of their own (a
+    # flush sits between the legs)
+    ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K2)]
     for s in range(K2):
         flush.zero_()
         ev3[s][0].record(stream)
         backward(True)
         ev3[s][1].record(stream)
+        flush.zero_()
+        ev3[s][2].record(stream)
+        decode_gqa(8)
+        ev3[s][3].record(stream)
+        flush.zero_()
+        ev3[s][4].record(stream)
+        decode_gqa(2)
+        ev3[s][5].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     st = F.fa_device_status(sp)
@@ -465,8 +498,11 @@ def ours(args, world, rank, local):
     t_packed = sum(e[3].elapsed_time(e[4]) for e in ev2) / K2
     t_bnc = sum(e[5].elapsed_time(e[6]) for e in ev2) / K2
     t_bc = sum(e[0].elapsed_time(e[1]) for e in ev3) / K2
-    t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed, t_bnc, t_bc = (
-        max_over_ranks(world, x) for x in (t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed, t_bnc, t_bc))
+    t_g8 = sum(e[2].elapsed_time(e[3]) for e in ev3) / K2
+    t_g2 = sum(e[4].elapsed_time(e[5]) for e in ev3) / K2
+    t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed, t_bnc, t_bc, t_g8, t_g2 = (
+        max_over_ranks(world, x)
+        for x in (t_nc, t_c, t_var, t_dec, t_store, t_chunk, t_chunk_c, t_packed, t_bnc, t_bc, t_g8, t_g2))
     # continuation FLOPs, causal bottom-right, halved-square convention of
     # the varlen leg: 4 d H (Lq (Lk - Lq) + Lq^2 / 2) per sequence
     f_chunk = sum(4.0 * cd * cH * (lq_ * (lk_ - lq_) + lq_ * lq_ / 2) for lq_, lk_ in zip(cl_q, cl_k))
@@ -480,6 +516,14 @@ def ours(args, world, rank, local):
     dec_bytes = kv_bytes + 2 * B5 * H5 * d5 * 2 + B5 * H5 * 4 + sum((L + 15) // 16 for L in lens) * 4
     gbs = dec_bytes / (t_dec * 1e-3) / 1e9
     peak_tf, peak_gbs, peak_src = load_peaks()
+
+    def gqa_leg(hkv_g, t):
+        # unique K/V bytes of the kv heads, plus q, o, LSE and table entries
+        b_ = (float(sum(lens)) * hkv_g * d5 * 2 * 2 + 2 * B5 * H5 * d5 * 2 + B5 * H5 * 4
+              + sum((L + 15) // 16 for L in lens) * 4)
+        g_ = b_ / (t * 1e-3) / 1e9
+        return {"ms": t, "gbs": g_, "frac_hbm": g_ / peak_gbs, "kv_heads": hkv_g, "query_heads_per_kv_head": H5 // hkv_g,
+                "path": "cuda cores" if H5 // hkv_g < 8 else "tensor cores"}
 
     if args.case != "all":
         if rank == 0:
@@ -595,6 +639,8 @@ def ours(args, world, rank, local):
             "backward_causal": {"ms": t_bc, "tflops": 2.5 * f_c / (t_bc * 1e-3) / 1e12,
                                 "tflops_executed": 3.5 * f_c / (t_bc * 1e-3) / 1e12,
                                 "frac_bf16_peak_executed": 3.5 * f_c / (t_bc * 1e-3) / 1e12 / peak_tf},
+            "paged_decode_gqa_8kv": gqa_leg(8, t_g8),
+            "paged_decode_gqa_2kv": gqa_leg(2, t_g2),
         },
         "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": tflops / peak_tf, "traffic": PREFILL_TRAFFIC_BYTES,
@@ -605,10 +651,10 @@ def ours(args, world, rank, local):
         "e2e": {"value": e2e_tflops * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "prefill legs with q,k,v copied from pinned host memory and O, LSE copied back each step; "
                         "steps double-buffered over copy-in, compute and copy-out streams"},
-        "gpu_launches": 5 * K + 4 * K2 + 6 * K2,
-        "follow_up_legs": f"store_kvcache, paged_prefill_chunk, same_chunk_contiguous_kv, qkvpacked_noncausal and "
-                          f"backward_(non)causal: {K2} steps of their own after the main timed loop, not in "
-                          f"ms_per_step or value",
+        "gpu_launches": 5 * K + 4 * K2 + 6 * K2 + 4 * K2,
+        "follow_up_legs": f"store_kvcache, paged_prefill_chunk, same_chunk_contiguous_kv, qkvpacked_noncausal, "
+                          f"backward_(non)causal and paged_decode_gqa_8kv / _2kv: {K2} steps of their own after the "
+                          f"main timed loop, not in ms_per_step or value",
         "clocks": clk,
         "wall_s_timed": wall,
     }
