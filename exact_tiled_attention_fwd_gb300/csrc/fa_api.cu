@@ -382,7 +382,7 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
     fa_status st = ensure_init(&err);
     if (st != FA_OK) return st;
     const int group = H / Hkv;
-    if (group >= fa::kDecodeTcMinGroup && group <= 2 * fa::kBlockM && static_cast<long long>(B) * Hkv <= 65535 &&
+    if (group >= fa::kDecodeTcMinGroup && group <= fa::kBlockM && static_cast<long long>(B) * Hkv <= 65535 &&
         (static_cast<long long>(num_pages) + 1) * page_size <= (1ll << 31) - 1) {
         // Large query groups: the tensor-core decode (the group's query heads
         // are the rows of a Q tile), then the combine step.

@@ -81,14 +81,19 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kMaxSlots = 6;
 
-template <int D>
+// DECODE (one query tile: a group of at most 128 heads) gives the second
+// tile's Q and P space to the K/V ring, which holds 5 tiles instead of 3 at
+// d = 128: decode streams each K/V tile past little work, so its speed is
+// set by the bytes in flight.
+template <int D, bool DECODE>
 struct PrefillSmem {
     static constexpr uint32_t kTile = kBlockM * D * 2;         // one Q, K or V tile
     static constexpr uint32_t kPTile = kBlockM * kBlockN * 2;  // one P tile
-    static constexpr int kSlots = D == 128 ? 3 : 6;            // K/V ring
+    static constexpr int kSmemTiles = DECODE ? 1 : kTiles;     // Q and P tiles held
+    static constexpr int kSlots = D == 128 ? (DECODE ? 5 : 3) : 6;  // K/V ring
     static constexpr uint32_t kQ = 0;                           // + t * kTile
-    static constexpr uint32_t kP = kQ + kTiles * kTile;         // + t * kPTile
-    static constexpr uint32_t kKV = kP + kTiles * kPTile;       // + slot * kTile
+    static constexpr uint32_t kP = kQ + kSmemTiles * kTile;     // + t * kPTile
+    static constexpr uint32_t kKV = kP + kSmemTiles * kPTile;   // + slot * kTile
     static constexpr uint32_t kBar = kKV + kSlots * kTile;
     static constexpr uint32_t kNumBars = 40;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
@@ -177,7 +182,7 @@ template <int D, bool CAUSAL, bool PAGED, bool DECODE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using L = PrefillSmem<D>;
+    using L = PrefillSmem<D, DECODE>;
     constexpr int kPanels = D / 64;
     constexpr int kSlots = L::kSlots;
     constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
@@ -214,6 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int kbeg = split * p.split_tokens;
         if (kbeg >= L) return;
+        if (p.decode_group > kBlockM) {  // one query tile: the shared-memory layout holds no second
+            if (threadIdx.x == 0 && split == 0) atomicOr(p.err, FA_DEVERR_INDEX);
+            return;
+        }
         Lk = min(p.split_tokens, L - kbeg);
         k_start = 0;
         q_start = seq * p.decode_group;
@@ -760,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool CAUSAL, bool PAGED, bool DECODE = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      cudaStream_t stream) {
-    using L = PrefillSmem<D>;
+    using L = PrefillSmem<D, DECODE>;
     static_assert(L::kDyn <= 232448u, "shared memory budget");
     static_assert(L::kSlots <= kMaxSlots, "K/V ring");
     auto kern = prefill_kernel<D, CAUSAL, PAGED, DECODE>;

@@ -200,7 +200,7 @@ size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen);
  *       it need not be initialised.
  * page_size must be 16.  causal is accepted; under bottom-right alignment it
  * does not change a single newest-token query.
- * Groups of H / Hkv >= 8 query heads per kv head (up to 256) run on the
+ * Groups of H / Hkv >= 8 query heads per kv head (up to 128) run on the
  * tensor cores: the group's query heads are the rows of one query tile, the
  * keys are taken in splits of 2048, and the splits are merged as in the
  * CUDA-core path.  Smaller groups use the CUDA-core split kernel.  The
