@@ -107,20 +107,41 @@ def test_gather_bit_exact(fa):
             assert np.array_equal(got[b, :L], ref), f"seq {b}"
 
 
-def test_bad_block_table_entry(fa):
-    """An entry outside the pool is skipped and reported; the other sequences
-    are unaffected."""
-    lens = [40, 40]
-    pb = W.paged_inputs(lens, 2, 64, 24, "cuda")
+@pytest.mark.parametrize("H,Hkv", [(2, 2), (16, 2)])
+def test_bad_block_table_entry(fa, H, Hkv):
+    """An entry outside the pool (or negative) is skipped and reported; the
+    other sequences are unaffected.  16 query heads per kv head take the
+    tensor-core decode."""
+    lens = [40, 40, 2100]
+    pb = W.paged_inputs(lens, H, 64, 24, "cuda", Hkv=Hkv)
     bt = pb.block_table.clone()
     bt[1, 1] = pb.num_pages + 100
+    bt[2, 130] = -7  # in the second 2048-key split
     pb2 = W.PagedBatch(pb.q, pb.k_cache, pb.v_cache, bt, pb.seqlens, pb.lengths, pb.max_seqlen, pb.num_pages)
-    o, lse = run_paged(fa, pb2, 2, 64, 0.125)
+    o, lse = run_paged(fa, pb2, H, 64, 0.125)
     assert fa.fa_device_status() == fa.FA_ERR_DEVICE_INDEX
     O_ref, L_ref = oracle.attention_paged(f64(pb.q), f64(pb.k_cache), f64(pb.v_cache), pb.block_table.cpu().numpy(),
                                           lens, 16, 0.125, True)
     assert_o_close(o[0:1], O_ref[0:1], "good sequence")
-    assert np.all(np.isfinite(f64(o[1])))
+    assert_lse_close(lse[0:1], L_ref[0:1], "good sequence")
+    assert np.all(np.isfinite(f64(o[1:])))
+
+
+def test_seqlen_beyond_max_reported(fa):
+    """A seqlens entry above max_seqlen is clamped to max_seqlen and reported,
+    on the CUDA-core path and on the tensor-core path."""
+    for H, Hkv in ((4, 4), (16, 2)):
+        lens = [100, 300]
+        pb = W.paged_inputs(lens, H, 64, 26, "cuda", Hkv=Hkv, slack_pages=4)
+        bad = pb.seqlens.clone()
+        bad[0] = pb.max_seqlen + 50
+        pb2 = W.PagedBatch(pb.q, pb.k_cache, pb.v_cache, pb.block_table, bad, pb.lengths, pb.max_seqlen, pb.num_pages)
+        o, lse = run_paged(fa, pb2, H, 64, 0.125)
+        assert fa.fa_device_status() == fa.FA_ERR_DEVICE_INDEX
+        O_ref, L_ref = oracle.attention_paged(f64(pb.q), f64(pb.k_cache), f64(pb.v_cache),
+                                              pb.block_table.cpu().numpy(), lens, 16, 0.125, True)
+        assert_o_close(o[1:2], O_ref[1:2], f"H{H}/{Hkv} good sequence")
+        assert np.all(np.isfinite(f64(o)))
 
 
 def test_deterministic(fa):
