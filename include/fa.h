@@ -39,8 +39,11 @@
  *  - Host-side validation runs before any launch and returns FA_ERR_INVALID
  *    or FA_ERR_UNSUPPORTED without touching the GPU.  Index arrays that live
  *    on the device (cu_seqlens, block_table, seqlens) are checked by the
- *    kernels: a bad entry is skipped (its keys are treated as absent) and
- *    recorded in a device error word that fa_device_status() reports.
+ *    kernels: a bad entry is never dereferenced (it is skipped, or its page
+ *    is read as zeros, as each entry point states) and is recorded in a
+ *    device error word that fa_device_status() reports.  The outputs of a
+ *    sequence with a bad entry are not meaningful; the other sequences are
+ *    unaffected.
  *  - Every wait inside a kernel is bounded in time; on expiry the kernel
  *    records FA_ERR_TIMEOUT in the device error word, drains its own copies,
  *    frees its tensor memory and returns.
@@ -190,8 +193,9 @@ size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen);
  *   block_table : int32 [B, max_pages_per_seq], DEVICE; logical token t of
  *       sequence b is page block_table[b][t / page_size], slot
  *       t % page_size.  Entries past ceil(seqlens[b] / page_size) are never
- *       read.  An entry outside [0, num_pages) is skipped and reported as
- *       FA_ERR_DEVICE_INDEX.
+ *       read.  An entry outside [0, num_pages) is reported as
+ *       FA_ERR_DEVICE_INDEX; the CUDA-core path skips its page, the
+ *       tensor-core path (groups of 8 or more, below) reads it as zeros.
  *   seqlens   : int32 [B], DEVICE; cached tokens per sequence, each in
  *       [0, max_seqlen] (0 gives O = 0, LSE = -inf).
  *   lse       : [B, H] fp32, may be NULL.
