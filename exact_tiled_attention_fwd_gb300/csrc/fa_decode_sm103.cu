@@ -6,14 +6,20 @@
 // of the dlog.com.cn page "从标准 Attention 到 FlashAttention 与分页执行",
 // §3.4 and its PagedAttention section).  Decode reads every cached byte once,
 // so the kernel is bound by HBM bandwidth, not by arithmetic: no tensor cores.
+// (Query groups of 8 or more heads per kv head decode on the tensor cores
+// instead, in the prefill kernel's decode mode, and share the combine kernel
+// below.)
 //
-// Split kernel: one warp per (sequence, head, split of split_tokens tokens).
-// A warp reads the split page by page with 16-byte loads; D/8 lanes hold one
-// key row (lane group g, element chunk c), so one warp instruction reads
-// 32/(D/8) whole rows, each a contiguous d*2-byte run.  Scores are the chunk
-// dot products summed across the row's lanes (xor shuffles); the running
-// (m, l, o) follow the online-softmax recurrence of the same page §2.2 with
-// the page as the block.  The split writes its unnormalised o and (m, l).
+// Split kernel: one warp per (sequence, split of split_tokens tokens, G query
+// heads of one kv head).  A warp reads the split page by page with 16-byte
+// loads; D/8 lanes hold one key row (lane group g, element chunk c), so one
+// warp instruction reads 32/(D/8) whole rows, each a contiguous d*2-byte run.
+// The next page's K/V lines are prefetched into L2 while a page is computed.
+// Scores are the chunk dot products summed across the row's lanes (xor
+// shuffles; for G > 1 a halving reduction that leaves one whole score per
+// lane); the running (m, l, o) follow the online-softmax recurrence of the
+// same page §2.2 with the page as the block.  The split writes its
+// unnormalised o and (m, l).
 //
 // Combine kernel: one warp per (sequence, head) merges the splits with the
 // same rescale rule: M = max m_s, w_s = 2^(m_s - M), l = sum w_s l_s,

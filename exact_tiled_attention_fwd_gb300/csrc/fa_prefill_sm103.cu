@@ -61,6 +61,20 @@
 // entirely above the diagonal are never loaded (tile skipping).  Query rows
 // past the sequence end are computed on whatever rows TMA brought in but
 // never stored.
+//
+// Variants (template parameters):
+//   PAGED   K/V come through a page table: the producer issues one 16-row box
+//           per page and panel, each lane one box, the table entries fetched
+//           a block ahead (prefill chunks that continue a cached prefix).
+//   DECODE  (with PAGED) single-token decode for a large query group: the
+//           group's query heads are the query rows of tile 0, grid.x splits
+//           the keys, and the epilogue writes each split's unnormalised O and
+//           (m, l) for the decode combine kernel; tile 1 is unused and its
+//           shared memory goes to a deeper K/V ring.
+// Dispatch order (cta_unit): non-causal CTAs run the Q blocks of a head
+// together; causal ones hand out the heaviest Q blocks first, at d = 128 in
+// groups of 8 heads so that few heads' K/V are live in L2 at once.  Dense
+// CTAs also prefetch into L2 the Q tiles of the CTA one wave later.
 
 #include <cstdint>
 #include <cuda.h>
