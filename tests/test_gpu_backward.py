@@ -146,3 +146,24 @@ def test_backward_workspace_too_small(fa):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     st = fa.fa_bwd(q, k, v, o, lse, q, dq, dk, dv, ws, ws.numel(), B, H, H, N, d, 0.125, 0)
     assert st == fa.FA_ERR_INVALID
+
+
+@pytest.mark.parametrize("causal,heads", [(False, (5, 18)), (True, (0, 27))])
+def test_backward_full_size_whole_heads(fa, causal, heads):
+    """The launch bench.py times (B1 H32 N8192 d128): every element of two
+    heads' dQ, dK and dV against the oracle's float64 gradients of those
+    heads, within the per-element bound above.  Heads are independent
+    (H = Hkv), so a head checked whole is checked exactly as in the full run."""
+    B, N, H, d = 1, 8192, 32, 128
+    q, k, v = W.dense_inputs(B, N, H, d, 1236, "cuda")
+    do = W.randn_bf16_device((B, N, H, d), 1236 * 7 + 1, "cuda")
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.attention(q, k, v, scale=scale, causal=causal)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    for h in heads:
+        ref, bnd = head_bounds(f64(q[0, :, h]), f64(k[0, :, h]), f64(v[0, :, h]), f64(do[0, :, h]), scale, causal)
+        got = [t[0, :, h] for t in (dq, dk, dv)]
+        assert_grads_close(got, ref, bnd, f"N8192 h{h} c{causal}")
+

@@ -88,6 +88,28 @@ def test_c5_sampled_heads(fa):
         assert_lse_close(lg[:, h:h + 1], L_ref, f"C5 h{h}")
 
 
+def test_c5_tensor_core_sampled_heads(fa):
+    """The full decode batch over 2 kv heads (16 query heads each, the
+    tensor-core path bench.py times): every sequence, sampled query heads of
+    both kv groups, checked by the oracle walking the real table over that
+    kv head's slice of the real pool."""
+    lens = W.c5_lengths()
+    H, Hkv, d = 32, 2, 128
+    pb = W.paged_inputs(lens, H, d, 1239 + Hkv, "cuda", Hkv=Hkv, pool_on_device=True)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_paged(fa, pb, H, d, scale)
+    assert fa.fa_device_status() == fa.FA_OK
+    og, lg = f64(o), f64(lse)
+    bt = pb.block_table.cpu().numpy()
+    for h in (0, 9, 16, 31):
+        hk = h // (H // Hkv)
+        kp = f64(pb.k_cache[:, :, hk:hk + 1, :])
+        vp = f64(pb.v_cache[:, :, hk:hk + 1, :])
+        O_ref, L_ref = oracle.attention_paged(f64(pb.q[:, h:h + 1]), kp, vp, bt, lens, 16, scale, True)
+        assert_o_close(og[:, h:h + 1], O_ref, f"C5 Hkv2 h{h}")
+        assert_lse_close(lg[:, h:h + 1], L_ref, f"C5 Hkv2 h{h}")
+
+
 def test_gather_bit_exact(fa):
     """The decode kernels' page walk reads exactly the bytes the host walk of
     block_table selects."""
