@@ -90,6 +90,32 @@ def check_paged(fa, lq, lk, H, Hkv, d, causal, seed, scale=None):
     assert_lse_close(lse, L_ref, what)
 
 
+def test_bench_chunk_full_size(fa):
+    """The continuation chunk bench.py times (16 sequences, cached context
+    U[512, 8192] + new tokens U[256, 2048], H32 d128, causal, pool on the
+    device): every query row of three sequences on two heads, against the
+    oracle's attention over keys gathered by its own host page walk."""
+    lq, lk = W.chunk_lengths()
+    H, d = W.CHUNK["H"], W.CHUNK["d"]
+    b = W.chunk_inputs(lq, lk, H, d, 1240, "cuda", stale=0.0, pool_on_device=True)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_paged(fa, b, H, H, d, scale, True)
+    og, lg = f64(o), f64(lse)
+    cu = b.cu_q.cpu().numpy()
+    bt = b.block_table.cpu().numpy()
+    for s in (int(np.argmax(lk)), int(np.argmin(lq)), 7):
+        a = int(cu[s])
+        for h in (4, 29):
+            kh = b.k_cache[:, :, h:h + 1].float().cpu().numpy()
+            vh = b.v_cache[:, :, h:h + 1].float().cpu().numpy()
+            K = oracle.gather_paged_kv(kh, bt[s], lk[s], PAGE)[:, 0]
+            Vv = oracle.gather_paged_kv(vh, bt[s], lk[s], PAGE)[:, 0]
+            O_ref, L_ref = oracle.attention_rows(f64(b.q[a:a + lq[s], h]), K, Vv, scale, True,
+                                                 rows=np.arange(lq[s]), Lq=lq[s])
+            assert_o_close(og[a:a + lq[s], h], O_ref, f"chunk s{s} h{h}")
+            assert_lse_close(lg[h, a:a + lq[s]], L_ref, f"chunk s{s} h{h}")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [True, False])
 def test_continuation_chunks(fa, d, causal):

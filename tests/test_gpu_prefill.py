@@ -70,6 +70,21 @@ def test_c3_sampled(fa, causal):
         assert_lse_close(lg[0, h, rows], L_ref, f"C3 h{h}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_c3_whole_heads(fa, causal):
+    """B1 H32 N8192 d128 at full size: every row of two heads (one in each
+    causal head group of 8) against the oracle's naive attention of the head."""
+    B, N, H, d = 1, 8192, 32, 128
+    q, k, v = W.dense_inputs(B, N, H, d, 1236, "cuda")
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_dense(fa, q, k, v, scale, causal)
+    og, lg = f64(o), f64(lse)
+    for h in (3, 30):
+        O_ref, L_ref = oracle.attention_head(f64(q[0, :, h]), f64(k[0, :, h]), f64(v[0, :, h]), scale, causal)
+        assert_o_close(og[0, :, h], O_ref, f"C3 whole head {h} c{causal}")
+        assert_lse_close(lg[0, h], L_ref, f"C3 whole head {h} c{causal}")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [1, 2, 63, 65, 127, 129, 1000])
 @pytest.mark.parametrize("causal", [False, True])

@@ -93,6 +93,26 @@ def test_c4_sampled(fa):
             assert_lse_close(lg[h, a + rows], L_ref, f"C4 s{s} h{h}")
 
 
+def test_c4_whole_sequences(fa):
+    """The full-size C4 launch: every row of the longest and the shortest
+    sequence, on three heads, against the oracle's naive causal attention of
+    that sequence alone."""
+    lens = W.c4_lengths()
+    H, d = 32, 64
+    q, k, v, cq, ck = W.varlen_inputs(lens, H, d, 1238, "cuda")
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_varlen(fa, q, k, v, cq, ck, lens, lens, scale, True)
+    og, lg = f64(o), f64(lse)
+    cu = cq.cpu().numpy()
+    for s in (int(np.argmax(lens)), int(np.argmin(lens))):
+        a, L = int(cu[s]), lens[s]
+        for h in (0, 13, 31):
+            O_ref, L_ref = oracle.attention_head(f64(q[a:a + L, h]), f64(k[a:a + L, h]), f64(v[a:a + L, h]), scale,
+                                                 True)
+            assert_o_close(og[a:a + L, h], O_ref, f"C4 whole s{s} h{h}")
+            assert_lse_close(lg[h, a:a + L], L_ref, f"C4 whole s{s} h{h}")
+
+
 def test_varlen_equals_dense_per_sequence(fa):
     """The GPU's varlen result for a sequence equals its dense result."""
     lens = [200, 77]
