@@ -88,13 +88,15 @@ def test_c5_sampled_heads(fa):
         assert_lse_close(lg[:, h:h + 1], L_ref, f"C5 h{h}")
 
 
-def test_c5_tensor_core_sampled_heads(fa):
-    """The full decode batch over 2 kv heads (16 query heads each, the
-    tensor-core path bench.py times): every sequence, sampled query heads of
-    both kv groups, checked by the oracle walking the real table over that
+@pytest.mark.parametrize("Hkv", [8, 2])
+def test_c5_grouped_sampled_heads(fa, Hkv):
+    """The full decode batch over 8 kv heads (4 query heads each, the
+    CUDA-core grouped warps) and over 2 kv heads (16 each, the tensor-core
+    path), as bench.py times them: every sequence, sampled query heads of
+    several kv groups, checked by the oracle walking the real table over that
     kv head's slice of the real pool."""
     lens = W.c5_lengths()
-    H, Hkv, d = 32, 2, 128
+    H, d = 32, 128
     pb = W.paged_inputs(lens, H, d, 1239 + Hkv, "cuda", Hkv=Hkv, pool_on_device=True)
     scale = 1.0 / np.sqrt(d)
     o, lse = run_paged(fa, pb, H, d, scale)
@@ -106,8 +108,8 @@ def test_c5_tensor_core_sampled_heads(fa):
         kp = f64(pb.k_cache[:, :, hk:hk + 1, :])
         vp = f64(pb.v_cache[:, :, hk:hk + 1, :])
         O_ref, L_ref = oracle.attention_paged(f64(pb.q[:, h:h + 1]), kp, vp, bt, lens, 16, scale, True)
-        assert_o_close(og[:, h:h + 1], O_ref, f"C5 Hkv2 h{h}")
-        assert_lse_close(lg[:, h:h + 1], L_ref, f"C5 Hkv2 h{h}")
+        assert_o_close(og[:, h:h + 1], O_ref, f"C5 Hkv{Hkv} h{h}")
+        assert_lse_close(lg[:, h:h + 1], L_ref, f"C5 Hkv{Hkv} h{h}")
 
 
 def test_gather_bit_exact(fa):
