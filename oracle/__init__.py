@@ -1,4 +1,4 @@
-"""Float64 CPU oracle for exact attention forward (test infrastructure only).
+"""Float64 CPU oracle for exact attention, forward and backward (test infrastructure only).
 
 Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline/reference arm
 may import this package; the CUDA library never does, and the two share no

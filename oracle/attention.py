@@ -1,4 +1,4 @@
-"""Float64 CPU oracle for exact attention forward.
+"""Float64 CPU oracle for exact attention (the forward, and its backward).
 
 TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
@@ -69,6 +69,15 @@ __all__ = [
     "attention_dense",
     "attention_varlen",
     "attention_paged",
+    "attention_varlen_paged",
+    "attention_qkvpacked",
+    "attention_kvpacked",
+    "attention_varlen_qkvpacked",
+    "attention_varlen_kvpacked",
+    "attention_backward_head",
+    "attention_backward_dense",
+    "attention_backward_varlen",
+    "store_kvcache",
     "gather_paged_kv",
     "visible_mask",
 ]
