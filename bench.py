@@ -46,6 +46,10 @@ SEED_C3 = 1236
 SEED_C4 = 1238
 SEED_C5 = 1239
 SEED_CHUNK = 1240
+SEED_C1 = 1234
+SEED_C2 = 1235
+C1 = dict(B=1, H=1, N=256, d=64)
+C2 = dict(B=4, H=16, N=2048, d=128)
 WORKLOAD = ("dense prefill B1 H32 N8192 d128 non-causal + causal (fa_fwd), packed varlen prefill 16 x U[128,4096] "
             "tokens H32 d64 causal (fa_varlen_fwd), then paged decode B64 H32 d128, KV lengths uniform in "
             "[512,16384], 16-token pages in a seeded random permutation (fa_paged_fwd); then a prefix-cache "
@@ -216,6 +220,42 @@ def cpu_baseline(budget_s: float = 20.0):
                       f"float64 numpy (BLAS default threads), {secs:.1f} s of CPU work"}
 
 
+def oracle_c1():
+    """The float64 oracle on the whole single-head case (B1 H1 N256 d64)."""
+    import numpy as np
+
+    import oracle
+    from exact_tiled_attention_fwd_gb300 import workloads as W
+
+    q, k, v = W.dense_inputs(C1["B"], C1["N"], C1["H"], C1["d"], SEED_C1, "cpu")
+    qh, kh, vh = (t[0, :, 0].float().numpy().astype(np.float64) for t in (q, k, v))
+    ts = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        oracle.attention_head(qh, kh, vh, 1.0 / math.sqrt(C1["d"]), False)
+        ts.append(time.perf_counter() - t0)
+    return {"us": statistics.median(ts) * 1e6, "sample": "the whole case, median of 5 runs", "cores": os.cpu_count()}
+
+
+def oracle_c2_sample():
+    """The float64 oracle on one whole head of the B4 H16 N2048 d128 prefill,
+    non-causal and causal."""
+    import numpy as np
+
+    import oracle
+    from exact_tiled_attention_fwd_gb300 import workloads as W
+
+    q, k, v = W.dense_inputs(C2["B"], C2["N"], C2["H"], C2["d"], SEED_C2, "cpu")
+    qh, kh, vh = (t[0, :, 0].float().numpy().astype(np.float64) for t in (q, k, v))
+    t0 = time.perf_counter()
+    oracle.attention_head(qh, kh, vh, 1.0 / math.sqrt(C2["d"]), False)
+    oracle.attention_head(qh, kh, vh, 1.0 / math.sqrt(C2["d"]), True)
+    dt = time.perf_counter() - t0
+    f = 4.0 * C2["N"] ** 2 * C2["d"] * 1.5
+    return {"tflops": f / dt / 1e12, "s": dt, "sample": "head 0 of sequence 0, non-causal + causal",
+            "cores": os.cpu_count()}
+
+
 def reference_arm(args, world, rank):
     """--impl reference: the float64 oracle on the host cores."""
     if rank != 0:
@@ -264,6 +304,7 @@ def ours(args, world, rank, local):
     do_chunk = args.case in ("all", "chunk")
     do_packed = args.case in ("all", "packed")
     do_bwd = args.case in ("all", "backward")
+    do_small = args.case in ("all", "small")
     q, k, v = W.dense_inputs(B, N, H, d, SEED_C3, dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -401,8 +442,36 @@ def ours(args, world, rank, local):
         if st != F.FA_OK:
             raise F.FAError(st, "fa_varlen_fwd (contiguous chunk)")
 
+    # the single-head case (B1 H1 N256 d64, non-causal) and the batched MHA
+    # prefill (B4 H16 N2048 d128, non-causal and causal)
+    q1, k1, v1 = W.dense_inputs(C1["B"], C1["N"], C1["H"], C1["d"], SEED_C1, dev)
+    o1 = torch.empty_like(q1)
+    l1 = torch.empty((C1["B"], C1["H"], C1["N"]), dtype=torch.float32, device=dev)
+    q2, k2, v2 = W.dense_inputs(C2["B"], C2["N"], C2["H"], C2["d"], SEED_C2, dev) if do_small else (q1, k1, v1)
+    o2 = torch.empty_like(q2)
+    l2 = torch.empty((q2.shape[0], q2.shape[2], q2.shape[1]), dtype=torch.float32, device=dev)
+
+    def small_c1():
+        if not do_small:
+            return
+        st = F.fa_fwd(q1, k1, v1, o1, l1, C1["B"], C1["H"], C1["H"], C1["N"], C1["d"], 1.0 / math.sqrt(C1["d"]),
+                      False, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_fwd (B1 H1 N256 d64)")
+
+    def small_c2(causal):
+        if not do_small:
+            return
+        st = F.fa_fwd(q2, k2, v2, o2, l2, C2["B"], C2["H"], C2["H"], C2["N"], C2["d"], 1.0 / math.sqrt(C2["d"]),
+                      causal, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_fwd (B4 H16 N2048 d128)")
+
     for _ in range(args.warmup):
         flush.zero_()
+        small_c1()
+        small_c2(False)
+        small_c2(True)
         prefill(False)
         prefill(True)
         varlen()
@@ -482,11 +551,35 @@ def ours(args, world, rank, local):
         ev3[s][4].record(stream)
         decode_gqa(2)
         ev3[s][5].record(stream)
+    # the two small configurations in a pass of their own: C1 call by call
+    # (its latency, the median of at least 20 calls), C2 with a flush
+    # before each leg
+    n1 = max(20, K2)
+    ev1 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n1)]
+    for s in range(n1):
+        flush.zero_()
+        ev1[s][0].record(stream)
+        small_c1()
+        ev1[s][1].record(stream)
+    ev4 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K2)]
+    for s in range(K2):
+        flush.zero_()
+        ev4[s][0].record(stream)
+        small_c2(False)
+        ev4[s][1].record(stream)
+        flush.zero_()
+        ev4[s][2].record(stream)
+        small_c2(True)
+        ev4[s][3].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     st = F.fa_device_status(sp)
     if st != F.FA_OK:
         raise F.FAError(st, "timed region")
+    t_c1 = statistics.median(e[0].elapsed_time(e[1]) for e in ev1)
+    t_c2 = sum(e[0].elapsed_time(e[1]) for e in ev4) / K2
+    t_c2c = sum(e[2].elapsed_time(e[3]) for e in ev4) / K2
+    t_c1, t_c2, t_c2c = (max_over_ranks(world, x) for x in (t_c1, t_c2, t_c2c))
 
     t_nc = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     t_c = sum(e[1].elapsed_time(e[2]) for e in ev) / K
@@ -525,9 +618,13 @@ def ours(args, world, rank, local):
         return {"ms": t, "gbs": g_, "frac_hbm": g_ / peak_gbs, "kv_heads": hkv_g, "query_heads_per_kv_head": H5 // hkv_g,
                 "path": "cuda cores" if H5 // hkv_g < 8 else "tensor cores"}
 
+    f_c1 = prefill_flops(C1["N"], C1["d"], C1["H"], C1["B"], False)
+    f_c2 = prefill_flops(C2["N"], C2["d"], C2["H"], C2["B"], False)
+    f_c2c = prefill_flops(C2["N"], C2["d"], C2["H"], C2["B"], True)
     if args.case != "all":
         if rank == 0:
             print(json.dumps({"case": args.case, "prefill_ms": [t_nc, t_c], "varlen_ms": t_var, "decode_ms": t_dec,
+                              "c1_us": t_c1 * 1e3, "c2_ms": [t_c2, t_c2c],
                               "prefill_tflops": tflops if do_prefill else None, "varlen_tflops": var_tflops,
                               "decode_gbs": gbs if do_decode else None,
                               "chunk_ms": [t_store, t_chunk, t_chunk_c],
@@ -641,6 +738,13 @@ def ours(args, world, rank, local):
                                 "frac_bf16_peak_executed": 3.5 * f_c / (t_bc * 1e-3) / 1e12 / peak_tf},
             "paged_decode_gqa_8kv": gqa_leg(8, t_g8),
             "paged_decode_gqa_2kv": gqa_leg(2, t_g2),
+            "c1_single_head_B1H1N256d64": {"us": t_c1 * 1e3, "tflops": f_c1 / (t_c1 * 1e-3) / 1e12,
+                                           "what": f"median of {n1} calls, each timed alone after an L2 flush; "
+                                                   "latency-bound (16.8 MFLOP)"},
+            "c2_noncausal_B4H16N2048d128": {"ms": t_c2, "tflops": f_c2 / (t_c2 * 1e-3) / 1e12,
+                                            "frac_bf16_peak": f_c2 / (t_c2 * 1e-3) / 1e12 / peak_tf},
+            "c2_causal_B4H16N2048d128": {"ms": t_c2c, "tflops": f_c2c / (t_c2c * 1e-3) / 1e12,
+                                         "frac_bf16_peak": f_c2c / (t_c2c * 1e-3) / 1e12 / peak_tf},
         },
         "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": tflops / peak_tf, "traffic": PREFILL_TRAFFIC_BYTES,
@@ -651,15 +755,17 @@ def ours(args, world, rank, local):
         "e2e": {"value": e2e_tflops * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "prefill legs with q,k,v copied from pinned host memory and O, LSE copied back each step; "
                         "steps double-buffered over copy-in, compute and copy-out streams"},
-        "gpu_launches": 5 * K + 4 * K2 + 6 * K2 + 4 * K2,
+        "gpu_launches": 5 * K + 4 * K2 + 6 * K2 + 4 * K2 + n1 + 2 * K2,
         "follow_up_legs": f"store_kvcache, paged_prefill_chunk, same_chunk_contiguous_kv, qkvpacked_noncausal, "
-                          f"backward_(non)causal and paged_decode_gqa_8kv / _2kv: {K2} steps of their own after the "
-                          f"main timed loop, not in ms_per_step or value",
+                          f"backward_(non)causal, paged_decode_gqa_8kv / _2kv and the C2 legs: {K2} steps of their "
+                          f"own after the main timed loop, C1: {n1} calls; none in ms_per_step or value",
         "clocks": clk,
         "wall_s_timed": wall,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+        line["legs"]["c1_single_head_B1H1N256d64"]["oracle"] = oracle_c1()
+        line["legs"]["c2_noncausal_B4H16N2048d128"]["oracle"] = oracle_c2_sample()
     print(json.dumps(line), flush=True)
 
 
@@ -671,7 +777,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode", "chunk", "packed", "backward"],
+    ap.add_argument("--case", choices=["all", "prefill", "varlen", "decode", "chunk", "packed", "backward", "small"],
                     default="all",
                     help="run only one leg (for profiling); prints a short line instead of the bench line")
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences of the decode leg (profiling)")

@@ -79,6 +79,22 @@ def randn_bf16_device(shape, seed: int, device) -> torch.Tensor:
     return torch.randn(shape, generator=g, dtype=torch.bfloat16, device=device)
 
 
+def sign_bf16(shape, seed: int, device="cpu") -> torch.Tensor:
+    """i.i.d. uniform signs (+1 or -1) as bf16, drawn on the CPU, then moved.
+    Used for key pools whose scores against a chosen key must be exact
+    integers (the one-hot gather tests)."""
+    t = torch.randint(0, 2, shape, generator=_gen(seed), dtype=torch.int16)
+    return (t * 2 - 1).to(torch.bfloat16).to(device)
+
+
+def sign_bf16_device(shape, seed: int, device) -> torch.Tensor:
+    """i.i.d. uniform signs as bf16, drawn directly on a CUDA device."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    t = torch.randint(0, 2, shape, generator=g, dtype=torch.int16, device=device)
+    return (t * 2 - 1).to(torch.bfloat16)
+
+
 def dense_inputs(B, N, H, d, seed: int, device="cpu", Hkv=None):
     """q [B, N, H, d], k, v [B, N, Hkv, d] bf16."""
     Hkv = H if Hkv is None else Hkv
@@ -125,9 +141,10 @@ class PagedBatch:
 
 
 def paged_inputs(lengths, H, d, seed: int, device="cpu", Hkv=None, page_size=PAGE_SIZE, slack_pages=0,
-                 pad_value=-1, pool_on_device=False, max_pages=None) -> PagedBatch:
+                 pad_value=-1, pool_on_device=False, max_pages=None, k_signs=False) -> PagedBatch:
     """A page pool holding every sequence's KV, pages assigned by a seeded
-    random permutation; unused block_table entries hold ``pad_value``."""
+    random permutation; unused block_table entries hold ``pad_value``.
+    ``k_signs`` draws the key pool as uniform signs instead of N(0, 1)."""
     Hkv = H if Hkv is None else Hkv
     B = len(lengths)
     pages_per = [(L + page_size - 1) // page_size for L in lengths]
@@ -141,10 +158,10 @@ def paged_inputs(lengths, H, d, seed: int, device="cpu", Hkv=None, page_size=PAG
         pos += n
     shape = (num_pages, page_size, Hkv, d)
     if pool_on_device:
-        kc = randn_bf16_device(shape, seed * 7 + 1, device)
+        kc = (sign_bf16_device if k_signs else randn_bf16_device)(shape, seed * 7 + 1, device)
         vc = randn_bf16_device(shape, seed * 7 + 2, device)
     else:
-        kc = randn_bf16(shape, seed * 7 + 1, device)
+        kc = (sign_bf16 if k_signs else randn_bf16)(shape, seed * 7 + 1, device)
         vc = randn_bf16(shape, seed * 7 + 2, device)
     q = randn_bf16((B, H, d), seed * 7 + 0, device)
     return PagedBatch(q, kc, vc, bt.to(device), torch.tensor(lengths, dtype=torch.int32).to(device),
@@ -175,11 +192,12 @@ class ChunkBatch:
 
 
 def chunk_inputs(lengths_q, lengths_k, H, d, seed: int, device="cpu", Hkv=None, page_size=PAGE_SIZE,
-                 slack_pages=0, stale=float("nan"), pool_on_device=False) -> ChunkBatch:
+                 slack_pages=0, stale=float("nan"), pool_on_device=False, k_signs=False) -> ChunkBatch:
     """A prefill chunk that continues cached prefixes: sequence s has
     lengths_k[s] keys in the page pool (pages in a seeded random permutation)
     and its lengths_q[s] newest tokens as queries.  Every slot no sequence
-    uses (the tail of each last page, the slack pages) holds ``stale``."""
+    uses (the tail of each last page, the slack pages) holds ``stale``.
+    ``k_signs`` draws the key pool as uniform signs instead of N(0, 1)."""
     Hkv = H if Hkv is None else Hkv
     S = len(lengths_k)
     pages_per = [(L + page_size - 1) // page_size for L in lengths_k]
@@ -196,10 +214,10 @@ def chunk_inputs(lengths_q, lengths_k, H, d, seed: int, device="cpu", Hkv=None, 
             used[int(bt[s, t // page_size]), : min(page_size, lengths_k[s] - t)] = True
     shape = (num_pages, page_size, Hkv, d)
     if pool_on_device:
-        kc = randn_bf16_device(shape, seed * 11 + 1, device)
+        kc = (sign_bf16_device if k_signs else randn_bf16_device)(shape, seed * 11 + 1, device)
         vc = randn_bf16_device(shape, seed * 11 + 2, device)
     else:
-        kc = randn_bf16(shape, seed * 11 + 1, device)
+        kc = (sign_bf16 if k_signs else randn_bf16)(shape, seed * 11 + 1, device)
         vc = randn_bf16(shape, seed * 11 + 2, device)
     if stale is not None:
         mask = (~used).to(kc.device)

@@ -228,9 +228,13 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
  * workspace_bytes.  The split-KV partials go to one fixed 16 MiB device array
  * inside this library, which every GPU that loads the library keeps until
  * the process exits.  The keys are split into as few pieces as needed for the
- * partials, B * H * splits * (d + 2) floats, to fit; a batch with
- * B * H * (d + 2) * 4 > 16 MiB - 256 bytes (for d = 128: B * H > 32,255)
- * returns FA_ERR_SCRATCH_CAPACITY.  Nothing in the array needs to start at
+ * partials, B * H * splits * (d + 2) floats, to fit; 256 bytes of the array
+ * are kept back for alignment, so a batch with
+ * B * H * (d + 2) * 4 > 16 MiB - 256 bytes returns FA_ERR_SCRATCH_CAPACITY
+ * before any launch (d = 128: at most 32,263 (sequence, head) pairs; d = 64:
+ * at most 63,549).  Every query group takes the CUDA-core split kernel here,
+ * including groups of 8 or more query heads per kv head, which fa_paged_fwd
+ * sends to the tensor cores; the results agree within the same tolerance.  Nothing in the array needs to start at
  * zero: every partial the combine step reads is written earlier in the same
  * call.  All calls in the process share the array, so two calls whose work
  * overlaps on the GPU (different streams, no ordering between them) race and
@@ -246,11 +250,13 @@ int fa_paged_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache
                          void* stream);
 
 /*
- * Copy, through the decode kernels' own page walk, the cached rows every
- * sequence would read: out[b][t][hk][:] = cache[block_table[b][t/16]][t%16][hk][:]
- * for t < seqlens[b].  out is bf16 [B, max_seqlen, Hkv, d] in DEVICE memory;
- * rows t >= seqlens[b] are left untouched.  A test and debugging aid for the
- * gather (a pure copy, so it must be bit-exact).
+ * Copy the cached rows every sequence's page walk selects:
+ * out[b][t][hk][:] = cache[block_table[b][t/16]][t%16][hk][:] for
+ * t < seqlens[b].  out is bf16 [B, max_seqlen, Hkv, d] in DEVICE memory;
+ * rows t >= seqlens[b] are left untouched.  A debugging aid: a kernel of its
+ * own that shares the decode kernel's page lookup and row offset, not the
+ * decode kernels themselves (their reads are checked bit for bit through
+ * fa_paged_fwd and fa_varlen_paged_fwd with one-hot queries).
  */
 int fa_paged_gather(const void* cache, const int* block_table, const int* seqlens, void* out,
                     int B, int Hkv, int d, int page_size, int num_pages,
