@@ -344,6 +344,8 @@ def ours(args, world, rank, local):
                            dtype=torch.int64, device=dev)
     c_kc = cb.k_cache.view(-1, cH, cd)[ck_rows].contiguous()
     c_vc = cb.v_cache.view(-1, cH, cd)[ck_rows].contiguous()
+    # the same chunk in a pool of 64-token pages (fewer, taller TMA boxes)
+    cb64 = W.chunk_inputs(cl_q, cl_k, cH, cd, SEED_CHUNK + 64, dev, stale=0.0, pool_on_device=True, page_size=64)
 
     def prefill(causal):
         if not do_prefill:
@@ -434,6 +436,15 @@ def ours(args, world, rank, local):
         if st != F.FA_OK:
             raise F.FAError(st, "fa_varlen_paged_fwd")
 
+    def chunk_page64():
+        if not do_chunk:
+            return
+        st = F.fa_varlen_paged_fwd(cb64.q, cb64.k_cache, cb64.v_cache, co, clse, cb64.cu_q, cb64.cu_k,
+                                   cb64.block_table, len(cl_q), cb64.max_q, cb64.max_k, c_tq, cH, cH, cd, 64,
+                                   cb64.num_pages, cb64.block_table.shape[1], 1.0 / math.sqrt(cd), True, sp)
+        if st != F.FA_OK:
+            raise F.FAError(st, "fa_varlen_paged_fwd (64-token pages)")
+
     def chunk_contiguous():
         if not do_chunk:
             return
@@ -478,6 +489,7 @@ def ours(args, world, rank, local):
         decode()
         store()
         chunk()
+        chunk_page64()
         chunk_contiguous()
         packed()
         backward(False)
@@ -518,7 +530,7 @@ def ours(args, world, rank, local):
     # the main one, so that their power draw does not change the clocks the
     # main legs run at.
     K2 = min(K, 100)
-    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K2)]
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(K2)]
     for s in range(K2):
         flush.zero_()
         e = ev2[s]
@@ -535,6 +547,10 @@ def ours(args, world, rank, local):
         e[5].record(stream)
         backward(False)
         e[6].record(stream)
+        flush.zero_()
+        e[7].record(stream)
+        chunk_page64()
+        e[8].record(stream)
     # the causal backward and the grouped decodes in a pass of their own (a
     # flush sits between the legs)
     ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K2)]
@@ -590,6 +606,7 @@ def ours(args, world, rank, local):
     t_chunk_c = sum(e[2].elapsed_time(e[3]) for e in ev2) / K2
     t_packed = sum(e[3].elapsed_time(e[4]) for e in ev2) / K2
     t_bnc = sum(e[5].elapsed_time(e[6]) for e in ev2) / K2
+    t_chunk64 = max_over_ranks(world, sum(e[7].elapsed_time(e[8]) for e in ev2) / K2)
     t_bc = sum(e[0].elapsed_time(e[1]) for e in ev3) / K2
     t_g8 = sum(e[2].elapsed_time(e[3]) for e in ev3) / K2
     t_g2 = sum(e[4].elapsed_time(e[5]) for e in ev3) / K2
@@ -627,7 +644,7 @@ def ours(args, world, rank, local):
                               "c1_us": t_c1 * 1e3, "c2_ms": [t_c2, t_c2c],
                               "prefill_tflops": tflops if do_prefill else None, "varlen_tflops": var_tflops,
                               "decode_gbs": gbs if do_decode else None,
-                              "chunk_ms": [t_store, t_chunk, t_chunk_c],
+                              "chunk_ms": [t_store, t_chunk, t_chunk_c, t_chunk64],
                               "chunk_tflops": f_chunk / (t_chunk * 1e-3) / 1e12 if do_chunk else None,
                               "chunk_contiguous_tflops": f_chunk / (t_chunk_c * 1e-3) / 1e12 if do_chunk else None,
                               "store_gbs": store_bytes / (t_store * 1e-3) / 1e9 if do_chunk else None,
@@ -725,6 +742,9 @@ def ours(args, world, rank, local):
             "paged_prefill_chunk": {"ms": t_chunk, "tflops": f_chunk / (t_chunk * 1e-3) / 1e12,
                                     "frac_bf16_peak": f_chunk / (t_chunk * 1e-3) / 1e12 / peak_tf,
                                     "new_tokens": c_tq, "cached_plus_new_tokens": int(sum(cl_k))},
+            "paged_prefill_chunk_page64": {"ms": t_chunk64, "tflops": f_chunk / (t_chunk64 * 1e-3) / 1e12,
+                                           "frac_bf16_peak": f_chunk / (t_chunk64 * 1e-3) / 1e12 / peak_tf,
+                                           "vs_contiguous": t_chunk64 / t_chunk_c},
             "same_chunk_contiguous_kv": {"ms": t_chunk_c, "tflops": f_chunk / (t_chunk_c * 1e-3) / 1e12},
             "qkvpacked_noncausal": {"ms": t_packed, "tflops": f_nc / (t_packed * 1e-3) / 1e12,
                                     "frac_bf16_peak": f_nc / (t_packed * 1e-3) / 1e12 / peak_tf},
@@ -755,8 +775,9 @@ def ours(args, world, rank, local):
         "e2e": {"value": e2e_tflops * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "prefill legs with q,k,v copied from pinned host memory and O, LSE copied back each step; "
                         "steps double-buffered over copy-in, compute and copy-out streams"},
-        "gpu_launches": 5 * K + 4 * K2 + 6 * K2 + 4 * K2 + n1 + 2 * K2,
-        "follow_up_legs": f"store_kvcache, paged_prefill_chunk, same_chunk_contiguous_kv, qkvpacked_noncausal, "
+        "gpu_launches": 5 * K + 5 * K2 + 6 * K2 + 4 * K2 + n1 + 2 * K2,
+        "follow_up_legs": f"store_kvcache, paged_prefill_chunk (16- and 64-token pages), same_chunk_contiguous_kv, "
+                          f"qkvpacked_noncausal, "
                           f"backward_(non)causal, paged_decode_gqa_8kv / _2kv and the C2 legs: {K2} steps of their "
                           f"own after the main timed loop, C1: {n1} calls; none in ms_per_step or value",
         "clocks": clk,

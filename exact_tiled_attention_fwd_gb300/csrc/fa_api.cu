@@ -279,7 +279,7 @@ int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
         return FA_ERR_INVALID;
     if (static_cast<long long>(max_pages_per_seq) * page_size < max_seqlen_k) return FA_ERR_INVALID;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    if (page_size != fa::kPageSize) return FA_ERR_UNSUPPORTED;
+    if (!fa::page_size_ok(page_size)) return FA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
     // rows of the pool view, plus one page of zero fill past its end, must be
     // addressable by a 32-bit TMA coordinate
@@ -290,8 +290,8 @@ int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
     const long long pool_rows = static_cast<long long>(num_pages) * page_size;
     CUtensorMap tq, tk, tv;
     if ((st = make_map(&tq, q, d, H, total_q)) != FA_OK) return st;
-    if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, fa::kPageSize)) != FA_OK) return st;
-    if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, fa::kPageSize)) != FA_OK) return st;
+    if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, page_size)) != FA_OK) return st;
+    if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, page_size)) != FA_OK) return st;
     fa::PrefillParams p{};
     p.o = o;
     p.lse = lse;
@@ -314,6 +314,7 @@ int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
     p.block_table = block_table;
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;
+    p.page_shift = fa::page_shift(page_size);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the causal grid enumerates (256-row block, head) pairs in grid.x
     if (static_cast<long long>((p.num_q_blocks + 1) / 2) * H > 2147483647ll) return FA_ERR_UNSUPPORTED;
@@ -373,8 +374,9 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
         !scale_ok(scale))
         return FA_ERR_INVALID;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    if (page_size != fa::kPageSize) return FA_ERR_UNSUPPORTED;
+    if (!fa::page_size_ok(page_size)) return FA_ERR_UNSUPPORTED;
     if (static_cast<long long>(max_pages_per_seq) * page_size < max_seqlen) return FA_ERR_INVALID;
+    if ((static_cast<long long>(num_pages) + 1) * page_size > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;
     if (B > 65535) return FA_ERR_UNSUPPORTED;
     const size_t need = fa_paged_workspace_size(B, H, d, max_seqlen);
     if (need == 0 || workspace_bytes < need) return FA_ERR_INVALID;
@@ -382,15 +384,14 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
     fa_status st = ensure_init(&err);
     if (st != FA_OK) return st;
     const int group = H / Hkv;
-    if (group >= fa::kDecodeTcMinGroup && group <= fa::kBlockM && static_cast<long long>(B) * Hkv <= 65535 &&
-        (static_cast<long long>(num_pages) + 1) * page_size <= (1ll << 31) - 1) {
+    if (group >= fa::kDecodeTcMinGroup && group <= fa::kBlockM && static_cast<long long>(B) * Hkv <= 65535) {
         // Large query groups: the tensor-core decode (the group's query heads
         // are the rows of a Q tile), then the combine step.
         const long long pool_rows = static_cast<long long>(num_pages) * page_size;
         CUtensorMap tq, tk, tv;
         if ((st = make_map(&tq, q, d, 1, static_cast<long long>(B) * H)) != FA_OK) return st;
-        if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, fa::kPageSize)) != FA_OK) return st;
-        if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, fa::kPageSize)) != FA_OK) return st;
+        if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, page_size)) != FA_OK) return st;
+        if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, page_size)) != FA_OK) return st;
         const int T = fa::kDecodeTcSplitTokens;
         const int splits = max_seqlen > T ? (max_seqlen + T - 1) / T : 1;
         const size_t slots = static_cast<size_t>(B) * H * splits;
@@ -412,6 +413,7 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
         pp.block_table = block_table;
         pp.max_pages = max_pages_per_seq;
         pp.num_pages = num_pages;
+        pp.page_shift = fa::page_shift(page_size);
         pp.seqlens = seqlens;
         pp.decode_group = group;
         pp.split_tokens = T;
@@ -431,6 +433,7 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
         p.max_seqlen = max_seqlen;
         p.split_tokens = T;
         p.max_splits = splits;
+        p.page_shift = fa::page_shift(page_size);
         p.ws_o = ws_o;
         p.ws_ml = ws_ml;
         p.scale_log2 = pp.scale_log2;
@@ -457,6 +460,7 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
     p.max_seqlen = max_seqlen;
     p.split_tokens = fa::decode_split_tokens(max_seqlen);
     p.max_splits = fa::decode_max_splits(max_seqlen);
+    p.page_shift = fa::page_shift(page_size);
     const size_t slots = static_cast<size_t>(B) * H * p.max_splits;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((slots * d * sizeof(float) + 255) & ~size_t(255)));
@@ -480,8 +484,9 @@ int fa_paged_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache
         !scale_ok(scale))
         return FA_ERR_INVALID;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    if (page_size != fa::kPageSize) return FA_ERR_UNSUPPORTED;
+    if (!fa::page_size_ok(page_size)) return FA_ERR_UNSUPPORTED;
     if (static_cast<long long>(max_pages_per_seq) * page_size < max_seqlen) return FA_ERR_INVALID;
+    if ((static_cast<long long>(num_pages) + 1) * page_size > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;
     if (B > 65535) return FA_ERR_UNSUPPORTED;
     // Split the keys so that the per-split partials fit the fixed scratch:
     // each (sequence, head, split) slot takes d floats of O and two of (m, l).
@@ -493,7 +498,7 @@ int fa_paged_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache
     int split_tokens = fa::decode_split_tokens(max_seqlen);
     if (splits > fit) {
         split_tokens = (max_seqlen + fit - 1) / fit;
-        split_tokens = (split_tokens + fa::kPageSize - 1) / fa::kPageSize * fa::kPageSize;
+        split_tokens = (split_tokens + fa::kPageChunk - 1) / fa::kPageChunk * fa::kPageChunk;
         splits = (max_seqlen + split_tokens - 1) / split_tokens;
         if (splits < 1) splits = 1;
     }
@@ -523,6 +528,7 @@ int fa_paged_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache
     p.max_seqlen = max_seqlen;
     p.split_tokens = split_tokens;
     p.max_splits = splits;
+    p.page_shift = fa::page_shift(page_size);
     p.ws_o = static_cast<float*>(scratch);
     p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
     p.scale_log2 = scale * 1.4426950408889634f;
@@ -537,7 +543,8 @@ int fa_paged_gather(const void* cache, const int* block_table, const int* seqlen
     if (!aligned16(cache) || !aligned16(out)) return FA_ERR_INVALID;
     if (B < 1 || Hkv < 1 || num_pages < 1 || max_pages_per_seq < 1 || max_seqlen < 1) return FA_ERR_INVALID;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    if (page_size != fa::kPageSize || B > 65535) return FA_ERR_UNSUPPORTED;
+    if (!fa::page_size_ok(page_size) || B > 65535) return FA_ERR_UNSUPPORTED;
+    if ((static_cast<long long>(num_pages) + 1) * page_size > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;
     if (static_cast<long long>(max_pages_per_seq) * page_size < max_seqlen) return FA_ERR_INVALID;
     unsigned int* err = nullptr;
     fa_status st = ensure_init(&err);
@@ -553,6 +560,7 @@ int fa_paged_gather(const void* cache, const int* block_table, const int* seqlen
     p.num_pages = num_pages;
     p.max_pages = max_pages_per_seq;
     p.max_seqlen = max_seqlen;
+    p.page_shift = fa::page_shift(page_size);
     p.err = err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return finish(fa::launch_gather(p, s), s);

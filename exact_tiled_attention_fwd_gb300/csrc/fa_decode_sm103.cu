@@ -1,8 +1,9 @@
 // Paged single-token decode for sm_103a: split-KV partial attention over the
 // page pool, then a combine of the per-split results.
 //
-// The cache is a pool of 16-token pages, [num_pages, 16, Hkv, d]; token t of
-// sequence b is page block_table[b][t / 16], slot t % 16 (the paged KV read
+// The cache is a pool of pages of 16, 32, 64 or 128 tokens,
+// [num_pages, page, Hkv, d]; token t of sequence b is page
+// block_table[b][t / page], slot t % page (the paged KV read
 // of the dlog.com.cn page "从标准 Attention 到 FlashAttention 与分页执行",
 // §3.4 and its PagedAttention section).  Decode reads every cached byte once,
 // so the kernel is bound by HBM bandwidth, not by arithmetic: no tensor cores.
@@ -11,14 +12,15 @@
 // below.)
 //
 // Split kernel: one warp per (sequence, split of split_tokens tokens, G query
-// heads of one kv head).  A warp reads the split page by page with 16-byte
-// loads; D/8 lanes hold one key row (lane group g, element chunk c), so one
-// warp instruction reads 32/(D/8) whole rows, each a contiguous d*2-byte run.
-// The next page's K/V lines are prefetched into L2 while a page is computed.
+// heads of one kv head).  A warp reads the split in chunks of 16 tokens (a
+// page of 16, or a quarter of a 64-token page) with 16-byte loads; D/8 lanes
+// hold one key row (lane group g, element chunk c), so one warp instruction
+// reads 32/(D/8) whole rows, each a contiguous d*2-byte run.  The next
+// chunk's K/V lines are prefetched into L2 while a chunk is computed.
 // Scores are the chunk dot products summed across the row's lanes (xor
 // shuffles; for G > 1 a halving reduction that leaves one whole score per
 // lane); the running (m, l, o) follow the online-softmax recurrence of the
-// same page §2.2 with the page as the block.  The split writes its
+// same page §2.2 with the chunk as the block.  The split writes its
 // unnormalised o and (m, l).
 //
 // Combine kernel: one warp per (sequence, head) merges the splits with the
@@ -53,21 +55,24 @@ __device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
     return r;
 }
 
-// Offset (in elements) of token `slot` of page `page`, kv head hk, element 0.
-__device__ __forceinline__ size_t paged_row_offset(int page, int slot, int Hkv, int hk, int d) {
-    return ((static_cast<size_t>(page) * kPageSize + slot) * Hkv + hk) * static_cast<size_t>(d);
+// Offset (in elements) of pool row `row` (page * page size + slot), kv head
+// hk, element 0.
+__device__ __forceinline__ size_t paged_row_offset(int row, int Hkv, int hk, int d) {
+    return (static_cast<size_t>(row) * Hkv + hk) * static_cast<size_t>(d);
 }
 
-// Page of logical token block `pg` of sequence b, or -1 (recorded as an index
-// error) when the table entry is outside the pool.
-__device__ __forceinline__ int lookup_page(const int* block_table, int max_pages, int num_pages, int b, int pg,
-                                           unsigned int* err) {
-    const int page = __ldg(block_table + static_cast<size_t>(b) * max_pages + pg);
+// Pool row of the first token of 16-token chunk `ck` of sequence b (page
+// block_table[b][ck * 16 >> shift], slot ck * 16 within it), or -1 (recorded
+// as an index error) when the table entry is outside the pool.
+__device__ __forceinline__ int lookup_chunk(const int* block_table, int max_pages, int num_pages, int shift, int b,
+                                            int ck, unsigned int* err) {
+    const int t = ck * kPageChunk;
+    const int page = __ldg(block_table + static_cast<size_t>(b) * max_pages + (t >> shift));
     if (static_cast<unsigned>(page) >= static_cast<unsigned>(num_pages)) {
         atomicOr(err, FA_DEVERR_INDEX);
         return -1;
     }
-    return page;
+    return (page << shift) + (t & ((1 << shift) - 1));
 }
 
 __device__ __forceinline__ int clamp_seqlen(int L, int max_seqlen, unsigned int* err, bool report) {
@@ -109,7 +114,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(const DecodeParams p) {
     constexpr int LPR = D / 8;         // lanes per key row
     constexpr int RPI = 32 / LPR;      // rows per warp load
-    constexpr int NI = kPageSize / RPI;  // loads per lane per page (K and V each)
+    constexpr int NI = kPageChunk / RPI;  // loads per lane per chunk (K and V each)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.z;
@@ -150,32 +155,33 @@ __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(con
         for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
     }
 
-    // The page walk runs ahead of the loads: the K/V rows of the page kAhead
-    // pages on are pulled into L2 while this page is computed, and table
-    // entries are fetched one page before that, so a page's loads find their
-    // lines in L2 instead of waiting on a dependent table load and then on
-    // HBM.  Grouped warps, which compute longer per page, look two pages ahead
-    // (measured 4.5% faster with 4 heads per warp, no gain for one).
-    const int pg0 = t0 / kPageSize;
-    const int pg_end = (t1 + kPageSize - 1) / kPageSize;
+    // The chunk walk runs ahead of the loads: the K/V rows of the chunk
+    // kAhead chunks on are pulled into L2 while this chunk is computed, and
+    // table entries are fetched one chunk before that, so a chunk's loads find
+    // their lines in L2 instead of waiting on a dependent table load and then
+    // on HBM.  Grouped warps, which compute longer per chunk, look two chunks
+    // ahead (measured 4.5% faster with 4 heads per warp, no gain for one).
+    // Chunks never straddle a page: every page size is a multiple of 16.
+    const int pg0 = t0 / kPageChunk;
+    const int pg_end = (t1 + kPageChunk - 1) / kPageChunk;
     auto entry = [&](int pg) {
-        return pg < pg_end ? lookup_page(p.block_table, p.max_pages, p.num_pages, b, pg, p.err) : -1;
+        return pg < pg_end ? lookup_chunk(p.block_table, p.max_pages, p.num_pages, p.page_shift, b, pg, p.err) : -1;
     };
-    // L2 prefetch of one page of this warp's kv head: lane l takes the
-    // 128-byte lines l * kPf .. l * kPf + kPf - 1 of the page's K lines
+    // L2 prefetch of one chunk of this warp's kv head: lane l takes the
+    // 128-byte lines l * kPf .. l * kPf + kPf - 1 of the chunk's K lines
     // followed by its V lines (row = line / kLinesPerRow).
     constexpr int kLinesPerRow = D / 64;
-    constexpr int kLinesPerPage = kPageSize * kLinesPerRow;  // per tensor
-    constexpr int kPf = 2 * kLinesPerPage / 32;              // prefetches per lane
-    static_assert(kPf * 32 == 2 * kLinesPerPage, "page lines per lane");
-    auto prefetch_page = [&](int page) {
-        if (page < 0) return;
+    constexpr int kLinesPerPage = kPageChunk * kLinesPerRow;  // per tensor
+    constexpr int kPf = 2 * kLinesPerPage / 32;               // prefetches per lane
+    static_assert(kPf * 32 == 2 * kLinesPerPage, "chunk lines per lane");
+    auto prefetch_page = [&](int row0) {
+        if (row0 < 0) return;
 #pragma unroll
         for (int x = 0; x < kPf; ++x) {
             const int line = lane * kPf + x;
             const int tl = line % kLinesPerPage;
             const uint16_t* a = (line < kLinesPerPage ? kc : vc) +
-                                paged_row_offset(page, tl / kLinesPerRow, p.Hkv, hk, D) + (tl % kLinesPerRow) * 64;
+                                paged_row_offset(row0 + tl / kLinesPerRow, p.Hkv, hk, D) + (tl % kLinesPerRow) * 64;
             asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
         }
     };
@@ -186,22 +192,22 @@ __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(con
 #pragma unroll
     for (int a = 1; a < kAhead; ++a) prefetch_page(ent[a]);
     for (int pg = pg0; pg < pg_end; ++pg) {
-        const int page = ent[0];
+        const int prow = ent[0];  // pool row of the chunk's first token
 #pragma unroll
         for (int a = 0; a < kAhead; ++a) ent[a] = ent[a + 1];
-        if (page < 0) {  // outside the pool: skipped (and reported by entry())
+        if (prow < 0) {  // outside the pool: skipped (and reported by entry())
             ent[kAhead] = entry(pg + kAhead + 1);
             continue;
         }
         uint4 kv[NI], vv[NI];
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
-            const size_t off = paged_row_offset(page, i * RPI + g, p.Hkv, hk, D) + c * 8;
+            const size_t off = paged_row_offset(prow + i * RPI + g, p.Hkv, hk, D) + c * 8;
             kv[i] = ldg_stream(kc + off);
         }
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
-            const size_t off = paged_row_offset(page, i * RPI + g, p.Hkv, hk, D) + c * 8;
+            const size_t off = paged_row_offset(prow + i * RPI + g, p.Hkv, hk, D) + c * 8;
             vv[i] = ldg_stream(vc + off);
         }
         prefetch_page(ent[kAhead - 1]);
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(con
                 float mp = neg_inf();
     #pragma unroll
                 for (int i = 0; i < NI; ++i) {
-                    const int tok = pg * kPageSize + i * RPI + g;
+                    const int tok = pg * kPageChunk + i * RPI + g;
                     if (tok >= t1) s[i] = neg_inf();
                     mp = fmaxf(mp, s[i]);
                 }
@@ -282,7 +288,7 @@ __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(con
                         sv[0] += __shfl_xor_sync(0xffffffffu, sv[0], off);
                     }
                 }
-                const int tok = pg * kPageSize + (c >> 1) * RPI + g;
+                const int tok = pg * kPageChunk + (c >> 1) * RPI + g;
                 sc[j] = tok < t1 ? sv[0] : neg_inf();
             }
             // Page maximum (lane pairs hold equal rows, so xor 1 is skipped),
@@ -400,25 +406,26 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_combine_kernel(const
 }
 
 // Pure copy of every row the decode kernel would read, through the same
-// page lookup and row offset.  grid = (pages of the longest sequence, B).
+// chunk lookup and row offset.  grid = (16-token chunks of the longest
+// sequence, B).
 __global__ void __launch_bounds__(256) gather_kernel(const GatherParams p) {
     const int b = blockIdx.y;
     const int pg = blockIdx.x;
     const int L = clamp_seqlen(__ldg(p.seqlens + b), p.max_seqlen, p.err, pg == 0 && threadIdx.x == 0);
-    if (pg * kPageSize >= L) return;
-    const int page = lookup_page(p.block_table, p.max_pages, p.num_pages, b, pg, p.err);
-    if (page < 0) return;
+    if (pg * kPageChunk >= L) return;
+    const int prow = lookup_chunk(p.block_table, p.max_pages, p.num_pages, p.page_shift, b, pg, p.err);
+    if (prow < 0) return;
     const int chunks = p.d / 8;                    // 16-byte chunks per row
     const int per_tok = p.Hkv * chunks;
-    const int ntok = min(kPageSize, L - pg * kPageSize);
+    const int ntok = min(kPageChunk, L - pg * kPageChunk);
     const uint16_t* src = static_cast<const uint16_t*>(p.cache);
     uint16_t* out = static_cast<uint16_t*>(p.out);
     for (int u = threadIdx.x; u < ntok * per_tok; u += blockDim.x) {
         const int slot = u / per_tok;
         const int hk = (u % per_tok) / chunks;
         const int cc = u % chunks;
-        const uint4 val = ldg_stream(src + paged_row_offset(page, slot, p.Hkv, hk, p.d) + cc * 8);
-        const size_t t = static_cast<size_t>(pg) * kPageSize + slot;
+        const uint4 val = ldg_stream(src + paged_row_offset(prow + slot, p.Hkv, hk, p.d) + cc * 8);
+        const size_t t = static_cast<size_t>(pg) * kPageChunk + slot;
         *reinterpret_cast<uint4*>(out + ((static_cast<size_t>(b) * p.max_seqlen + t) * p.Hkv + hk) * p.d + cc * 8) = val;
     }
 }
@@ -516,7 +523,7 @@ cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t str
 }
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
-    dim3 grid((p.max_seqlen + kPageSize - 1) / kPageSize, p.B);
+    dim3 grid((p.max_seqlen + kPageChunk - 1) / kPageChunk, p.B);
     gather_kernel<<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }

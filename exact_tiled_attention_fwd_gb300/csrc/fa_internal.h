@@ -17,8 +17,14 @@ namespace fa {
 // Query rows per tile, keys per K/V block of the prefill kernel.
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-// Tokens per page of the paged KV cache.
-constexpr int kPageSize = 16;
+// Tokens per page of the paged KV cache: 16, 32, 64 or 128 (a power of two
+// that divides the 128-key block).  Kernels take it as a shift.  The
+// CUDA-core decode walks every page in chunks of kPageChunk tokens.
+constexpr int kMinPageSize = 16;
+constexpr int kMaxPageSize = 128;
+constexpr int kPageChunk = 16;
+inline bool page_size_ok(int ps) { return ps == 16 || ps == 32 || ps == 64 || ps == 128; }
+inline int page_shift(int ps) { return ps == 16 ? 4 : ps == 32 ? 5 : ps == 64 ? 6 : 7; }
 
 struct PrefillParams {
     void* o;                 // bf16 [rows, H, d]
@@ -37,11 +43,12 @@ struct PrefillParams {
     unsigned long long wait_limit_ns;
     // Paged K/V (varlen only): when block_table is set, sequence s's keys are
     // the logical tokens 0 .. Lk-1 of its pages, token t at page
-    // block_table[s * max_pages + t / kPageSize], slot t % kPageSize, and the
-    // K/V tensor maps view the pool [num_pages * kPageSize, Hkv, d] with
-    // kPageSize-row boxes.
+    // block_table[s * max_pages + (t >> page_shift)], slot t % page size, and
+    // the K/V tensor maps view the pool [num_pages << page_shift, Hkv, d]
+    // with boxes of one page.
     const int* block_table;
     int max_pages, num_pages;
+    int page_shift;          // log2 of the page size
     // Grouped decode on the tensor cores (decode_group > 0, with a page
     // table): CTA (split, 0, s) takes the decode_group query heads of pair
     // s = (b, kv head) = (s / Hkv, s % Hkv) as its query rows (q viewed as
@@ -67,8 +74,9 @@ struct DecodeParams {
     float* ws_ml;            // fp32 [B, H, max_splits, 2] partial (m, l), log2 domain
     int B, H, Hkv, group;
     int num_pages, max_pages, max_seqlen;
-    int split_tokens;        // tokens per split (multiple of kPageSize)
+    int split_tokens;        // tokens per split (multiple of kPageChunk)
     int max_splits;
+    int page_shift;          // log2 of the page size
     float scale_log2;
     unsigned int* err;
 };
@@ -80,6 +88,7 @@ struct GatherParams {
     void* out;               // bf16 [B, max_seqlen, Hkv, d]
     int B, Hkv, d;
     int num_pages, max_pages, max_seqlen;
+    int page_shift;          // log2 of the page size
     unsigned int* err;
 };
 

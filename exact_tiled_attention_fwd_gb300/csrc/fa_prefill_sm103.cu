@@ -63,9 +63,10 @@
 // never stored.
 //
 // Variants (template parameters):
-//   PAGED   K/V come through a page table: the producer issues one 16-row box
-//           per page and panel, each lane one box, the table entries fetched
-//           a block ahead (prefill chunks that continue a cached prefix).
+//   PAGED   K/V come through a page table: the producer issues one box of a
+//           page's rows (16 to 128) per page and panel, each lane one box, the
+//           table entries fetched a block ahead (prefill chunks that continue
+//           a cached prefix).
 //   DECODE  (with PAGED) single-token decode for a large query group: the
 //           group's query heads are the query rows of tile 0, grid.x splits
 //           the keys, and the epilogue writes each split's unnormalised O and
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         k_start = 0;
         q_start = seq * p.decode_group;
         Lq = p.decode_group;
-        bt_row = p.block_table + static_cast<size_t>(b) * p.max_pages + kbeg / kPageSize;
+        bt_row = p.block_table + static_cast<size_t>(b) * p.max_pages + (kbeg >> p.page_shift);
     } else if (p.cu_q != nullptr) {
         q_start = p.cu_q[seq];
         Lq = p.cu_q[seq + 1] - q_start;
@@ -249,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         Lk = p.cu_k[seq + 1] - k_start;
         const bool bad = q_start < 0 || Lq < 0 || Lk < 0 || q_start + Lq > p.total_q || Lq > p.max_seqlen_q ||
                          Lk > p.max_seqlen_k ||
-                         (PAGED ? Lk > p.max_pages * kPageSize : (k_start < 0 || k_start + Lk > p.total_k));
+                         (PAGED ? Lk > (static_cast<long long>(p.max_pages) << p.page_shift)
+                                : (k_start < 0 || k_start + Lk > p.total_k));
         if (bad) {
             if (threadIdx.x == 0 && qb == 0) atomicOr(p.err, FA_DEVERR_INDEX);
             return;
@@ -273,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Paged keys whose last page is only partly used: the stale slots past Lk
     // are loaded with the page, and their V rows are zeroed before the last
     // P.V (P is 0 there, but 0 * a non-finite stale value would not be).
-    const bool v_tail = PAGED && (Lk % kPageSize) != 0 && nmax > 0 && (Lk - 1) / kBlockN == nmax - 1;
+    const int page_rows = PAGED ? 1 << p.page_shift : 1;  // tokens per page
+    const bool v_tail = PAGED && (Lk & (page_rows - 1)) != 0 && nmax > 0 && (Lk - 1) / kBlockN == nmax - 1;
     const long long lse_base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
@@ -419,21 +422,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Paged K/V: the whole warp runs the loop (its waits are
                 // warp-uniform); lane 0 posts the slot's byte count and each
                 // lane issues one page box (page lane / kPanels, panel
-                // lane % kPanels), so one instruction issues a whole tile.  A
-                // page past the sequence, or a bad table entry, is loaded from
-                // just past the pool: TMA fills zeros there (and still counts
-                // the bytes).
-                constexpr int kPagesPerBlock = kBlockN / kPageSize;
-                const int pg = lane / kPanels;  // this lane's page of a block
-                const int pn = lane % kPanels;  // and panel
-                const bool boxes = lane < kPagesPerBlock * kPanels;
+                // lane % kPanels), so one instruction issues a whole tile:
+                // 16 boxes at d = 128 with 16-token pages, 2 with 128-token
+                // pages.  A page past the sequence, or a bad table entry, is
+                // loaded from just past the pool: TMA fills zeros there (and
+                // still counts the bytes).
+                const int ppb = kBlockN >> p.page_shift;  // pages per 128-key block
+                const int pg = lane / kPanels;             // this lane's page of a block
+                const int pn = lane % kPanels;             // and panel
+                const bool boxes = lane < ppb * kPanels;
                 const int* bt = bt_row;
                 // Table entries are fetched one block ahead of their use: the
                 // entries of blocks j and j + 1 are in flight at once, kept by
                 // block parity.
                 auto fetch = [&](int blk) {
-                    return (boxes && blk < nmax && blk * kBlockN + pg * kPageSize < Lk)
-                               ? __ldg(bt + blk * kPagesPerBlock + pg)
+                    return (boxes && blk < nmax && blk * kBlockN + pg * page_rows < Lk)
+                               ? __ldg(bt + blk * ppb + pg)
                                : -1;
                 };
                 int ent0 = fetch(0), ent1 = fetch(1);
@@ -453,14 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (boxes) {
                         const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
                         const int page = (j & 1) ? ent1 : ent0;
-                        int row = p.num_pages * kPageSize;
-                        if (j * kBlockN + pg * kPageSize < Lk) {
+                        int row = p.num_pages << p.page_shift;
+                        if (j * kBlockN + pg * page_rows < Lk) {
                             if (page >= 0 && page < p.num_pages)
-                                row = page * kPageSize;
+                                row = page << p.page_shift;
                             else if (pn == 0 && is_k)
                                 atomicOr(p.err, FA_DEVERR_INDEX);
                         }
-                        tma_load_3d(sbase + L::kKV + s * L::kTile + pn * kPanelBytes + pg * kPageSize * 128, map,
+                        tma_load_3d(sbase + L::kKV + s * L::kTile + pn * kPanelBytes + pg * page_rows * 128, map,
                                     bar(B_KV_FULL + s), pn * 64, hk, row);
                     }
                     __syncwarp();
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (warp_wait(bar(B_KV_FULL + i_last % kSlots), (i_last / kSlots) & 1, abort_flag, p.err, lim)) {
                     const int kb = (nmax - 1) * kBlockN;
                     const int r_lo = Lk - kb;
-                    const int r_hi = ((Lk + kPageSize - 1) / kPageSize) * kPageSize - kb;
+                    const int r_hi = ((Lk + page_rows - 1) & ~(page_rows - 1)) - kb;
                     const uint32_t base = sbase + L::kKV + (i_last % kSlots) * L::kTile;
                     for (int e = lane; e < (r_hi - r_lo) * kPanels * 8; e += 32) {
                         const int chunk = e & 7;

@@ -154,7 +154,10 @@ int fa_varlen_kvpacked_fwd(const void* q, const void* kv, void* o, float* lse,
  *   max_seqlen_q, max_seqlen_k : bounds as in fa_varlen_fwd;
  *       max_pages_per_seq * page_size >= max_seqlen_k.
  *   lse : [H, total_q] fp32, may be NULL.
- * page_size must be 16.
+ * page_size is 16, 32, 64 or 128 (else FA_ERR_UNSUPPORTED); each page is
+ * read as one TMA box per 64-element panel, so larger pages take fewer boxes
+ * per 128-key block (16 at d = 128 with 16-token pages, 2 with 128-token
+ * pages).  (num_pages + 1) * page_size must stay below 2^31.
  */
 int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                         const int* cu_seqlens_q, const int* cu_seqlens_k, const int* block_table,
@@ -202,8 +205,10 @@ size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen);
  *   workspace : DEVICE scratch of at least
  *       fa_paged_workspace_size(B, H, d, max_seqlen) bytes, 16-byte aligned;
  *       it need not be initialised.
- * page_size must be 16.  causal is accepted; under bottom-right alignment it
- * does not change a single newest-token query.
+ * page_size is 16, 32, 64 or 128 (else FA_ERR_UNSUPPORTED), and
+ * (num_pages + 1) * page_size must stay below 2^31.  causal is accepted;
+ * under bottom-right alignment it does not change a single newest-token
+ * query.
  * Groups of H / Hkv >= 8 query heads per kv head (up to 128) run on the
  * tensor cores: the group's query heads are the rows of one query tile, the
  * keys are taken in splits of 2048, and the splits are merged as in the
@@ -251,7 +256,7 @@ int fa_paged_fwd_noalloc(const void* q, const void* k_cache, const void* v_cache
 
 /*
  * Copy the cached rows every sequence's page walk selects:
- * out[b][t][hk][:] = cache[block_table[b][t/16]][t%16][hk][:] for
+ * out[b][t][hk][:] = cache[block_table[b][t/page_size]][t%page_size][hk][:] for
  * t < seqlens[b].  out is bf16 [B, max_seqlen, Hkv, d] in DEVICE memory;
  * rows t >= seqlens[b] are left untouched.  A debugging aid: a kernel of its
  * own that shares the decode kernel's page lookup and row offset, not the

@@ -73,9 +73,13 @@ def test_validation_without_gpu(lib):
     assert lib.fa_varlen_fwd(A, A, A, A, None, A, A, 0, 8, 8, 8, 8, 1, 1, 128, 0.1, 0, S) == lib.FA_ERR_INVALID
     ws = lib.fa_paged_workspace_size(2, 4, 128, 100)
     assert ws > 0
-    # page size other than 16, too-small workspace, too few pages per sequence
-    assert lib.fa_paged_fwd(A, A, A, A, A, A, None, 2, 4, 4, 128, 32, 10, 8, 100, 0.1, 1, A, ws, S) == \
-        lib.FA_ERR_UNSUPPORTED
+    # page size not in {16, 32, 64, 128}, too-small workspace, too few pages
+    # per sequence
+    for ps in (8, 48, 256):
+        assert lib.fa_paged_fwd(A, A, A, A, A, A, None, 2, 4, 4, 128, ps, 10, 8, 100, 0.1, 1, A, ws, S) == \
+            lib.FA_ERR_UNSUPPORTED
+        assert lib.fa_paged_fwd_noalloc(A, A, A, A, A, A, None, 2, 4, 4, 128, ps, 10, 8, 100, 0.1, 1, S) == \
+            lib.FA_ERR_UNSUPPORTED
     assert lib.fa_paged_fwd(A, A, A, A, A, A, None, 2, 4, 4, 128, 16, 10, 8, 100, 0.1, 1, A, ws - 1, S) == \
         lib.FA_ERR_INVALID
     assert lib.fa_paged_fwd(A, A, A, A, A, A, None, 2, 4, 4, 128, 16, 10, 6, 100, 0.1, 1, A, ws, S) == \
@@ -88,7 +92,10 @@ def test_validation_without_gpu(lib):
     vp = lib.fa_varlen_paged_fwd
     assert vp(A, A, A, A, None, A, A, 0, 2, 64, 200, 64, 4, 2, 128, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_INVALID
     assert vp(A, A, A, A, None, A + 2, A, A, 2, 64, 200, 64, 4, 2, 128, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_INVALID
-    assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 128, 32, 30, 13, 0.1, 1, S) == lib.FA_ERR_UNSUPPORTED
+    assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 128, 48, 30, 13, 0.1, 1, S) == lib.FA_ERR_UNSUPPORTED
+    assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 128, 256, 30, 13, 0.1, 1, S) == lib.FA_ERR_UNSUPPORTED
+    # 32-token pages: 7 pages per sequence hold only 224 < 250 keys
+    assert vp(A, A, A, A, None, A, A, A, 2, 64, 250, 64, 4, 2, 128, 32, 30, 7, 0.1, 1, S) == lib.FA_ERR_INVALID
     assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 128, 16, 30, 12, 0.1, 1, S) == lib.FA_ERR_INVALID
     assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 3, 128, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_INVALID
     assert vp(A, A, A, A, None, A, A, A, 2, 64, 200, 64, 4, 2, 96, 16, 30, 13, 0.1, 1, S) == lib.FA_ERR_UNSUPPORTED

@@ -67,25 +67,26 @@ def test_store_kvcache_empty(fa):
 
 def run_paged(fa, b, H, Hkv, d, scale, causal):
     total_q = int(b.cu_q[-1])
+    ps = b.k_cache.shape[1]
     o = torch.full((total_q, H, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((H, total_q), float("nan"), dtype=torch.float32, device="cuda")
     st = fa.fa_varlen_paged_fwd(b.q, b.k_cache, b.v_cache, o, lse, b.cu_q, b.cu_k, b.block_table,
-                                len(b.lengths_q), b.max_q, b.max_k, total_q, H, Hkv, d, PAGE, b.num_pages,
+                                len(b.lengths_q), b.max_q, b.max_k, total_q, H, Hkv, d, ps, b.num_pages,
                                 b.block_table.shape[1], scale, causal)
     assert st == fa.FA_OK, fa.status_string(st)
     assert fa.fa_device_status() == fa.FA_OK
     return o, lse
 
 
-def check_paged(fa, lq, lk, H, Hkv, d, causal, seed, scale=None):
-    b = W.chunk_inputs(lq, lk, H, d, seed, "cuda", Hkv=Hkv, slack_pages=2)
+def check_paged(fa, lq, lk, H, Hkv, d, causal, seed, scale=None, page_size=PAGE):
+    b = W.chunk_inputs(lq, lk, H, d, seed, "cuda", Hkv=Hkv, slack_pages=2, page_size=page_size)
     scale = 1.0 / np.sqrt(d) if scale is None else scale
     o, lse = run_paged(fa, b, H, Hkv, d, scale, causal)
     O_ref, L_ref = oracle.attention_varlen_paged(f64(b.q), b.k_cache.float().cpu().numpy(),
                                                  b.v_cache.float().cpu().numpy(), b.cu_q.cpu().numpy(),
-                                                 b.cu_k.cpu().numpy(), b.block_table.cpu().numpy(), PAGE, scale,
+                                                 b.cu_k.cpu().numpy(), b.block_table.cpu().numpy(), page_size, scale,
                                                  causal)
-    what = f"lq{lq} lk{lk} H{H}/{Hkv} d{d} c{causal}"
+    what = f"lq{lq} lk{lk} H{H}/{Hkv} d{d} c{causal} page {page_size}"
     assert_o_close(o, O_ref, what)
     assert_lse_close(lse, L_ref, what)
 
@@ -124,6 +125,18 @@ def test_continuation_chunks(fa, d, causal):
     lk = [300, 129, 1000, 17, 16, 700]
     lq = [40, 129, 257, 1, 16, 128]
     check_paged(fa, lq, lk, 4, 2, d, causal, seed=21 + d)
+
+
+@pytest.mark.parametrize("page_size", [32, 64, 128])
+@pytest.mark.parametrize("d", [64, 128])
+def test_continuation_chunks_page_sizes(fa, page_size, d):
+    """Pages of 32, 64 and 128 tokens (one TMA box per page and panel; at
+    128 a page is a whole key block): ragged chunks, partly used last pages
+    holding NaN."""
+    lk = [300, 129, 1000, 17, 16, 700, 2 * page_size + 3]
+    lq = [40, 129, 257, 1, 16, 128, page_size]
+    check_paged(fa, lq, lk, 4, 2, d, True, seed=51 + d + page_size, page_size=page_size)
+    check_paged(fa, lq, lk, 4, 4, d, False, seed=52 + d + page_size, page_size=page_size)
 
 
 @pytest.mark.parametrize("d", [64, 128])

@@ -14,25 +14,37 @@ pytestmark = pytest.mark.gpu
 def run_paged(fa, pb, H, d, scale, causal=True):
     B = pb.q.shape[0]
     Hkv = pb.k_cache.shape[2]
+    ps = pb.k_cache.shape[1]
     o = torch.full_like(pb.q, float("nan"))
     lse = torch.full((B, H), float("nan"), dtype=torch.float32, device=pb.q.device)
     ws_bytes = fa.fa_paged_workspace_size(B, H, d, pb.max_seqlen)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=pb.q.device)
-    st = fa.fa_paged_fwd(pb.q, pb.k_cache, pb.v_cache, pb.block_table, pb.seqlens, o, lse, B, H, Hkv, d, 16,
+    st = fa.fa_paged_fwd(pb.q, pb.k_cache, pb.v_cache, pb.block_table, pb.seqlens, o, lse, B, H, Hkv, d, ps,
                          pb.num_pages, pb.block_table.shape[1], pb.max_seqlen, scale, causal, ws, ws_bytes)
     assert st == fa.FA_OK, fa.status_string(st)
     return o, lse
 
 
-def check_full(fa, lengths, H, d, seed, Hkv=None, slack=3):
-    pb = W.paged_inputs(lengths, H, d, seed, "cuda", Hkv=Hkv, slack_pages=slack)
+def check_full(fa, lengths, H, d, seed, Hkv=None, slack=3, page_size=16):
+    pb = W.paged_inputs(lengths, H, d, seed, "cuda", Hkv=Hkv, slack_pages=slack, page_size=page_size)
     scale = 1.0 / np.sqrt(d)
     o, lse = run_paged(fa, pb, H, d, scale)
     assert fa.fa_device_status() == fa.FA_OK
     O_ref, L_ref = oracle.attention_paged(f64(pb.q), f64(pb.k_cache), f64(pb.v_cache), pb.block_table.cpu().numpy(),
-                                          lengths, 16, scale, True)
-    assert_o_close(o, O_ref, f"paged {lengths}")
-    assert_lse_close(lse, L_ref, f"paged {lengths}")
+                                          lengths, page_size, scale, True)
+    assert_o_close(o, O_ref, f"paged {lengths} page {page_size}")
+    assert_lse_close(lse, L_ref, f"paged {lengths} page {page_size}")
+
+
+@pytest.mark.parametrize("page_size", [32, 64, 128])
+@pytest.mark.parametrize("H,Hkv,d", [(4, 4, 128), (8, 2, 64), (32, 2, 128), (32, 4, 64)])
+def test_page_sizes(fa, page_size, H, Hkv, d):
+    """Pages of 32, 64 and 128 tokens: lengths below, at and just past a
+    page, and across the 512- and 2048-token splits, on the CUDA-core split
+    kernel (groups of 1 and 4) and the tensor-core decode (groups of 16 and
+    8)."""
+    lens = [1, page_size - 1, page_size, page_size + 1, 513, 2 * page_size + 7, 2049, 4500, 0]
+    check_full(fa, lens, H, d, seed=40 + page_size + H + Hkv + d, Hkv=Hkv, page_size=page_size)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -112,14 +124,15 @@ def test_c5_grouped_sampled_heads(fa, Hkv):
         assert_lse_close(lg[:, h:h + 1], L_ref, f"C5 Hkv{Hkv} h{h}")
 
 
-def test_gather_bit_exact(fa):
-    """The decode kernels' page walk reads exactly the bytes the host walk of
-    block_table selects."""
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_gather_bit_exact(fa, page_size):
+    """fa_paged_gather (a copy kernel sharing the decode kernel's chunk
+    lookup) reads exactly the bytes the host walk of block_table selects."""
     lens = [1, 16, 17, 250, 999, 2048]
-    pb = W.paged_inputs(lens, 4, 128, 23, "cuda", slack_pages=5)
+    pb = W.paged_inputs(lens, 4, 128, 23, "cuda", slack_pages=5, page_size=page_size)
     for cache in (pb.k_cache, pb.v_cache):
         out = torch.zeros((len(lens), pb.max_seqlen, 4, 128), dtype=torch.bfloat16, device="cuda")
-        st = fa.fa_paged_gather(cache, pb.block_table, pb.seqlens, out, len(lens), 4, 128, 16, pb.num_pages,
+        st = fa.fa_paged_gather(cache, pb.block_table, pb.seqlens, out, len(lens), 4, 128, page_size, pb.num_pages,
                                 pb.block_table.shape[1], pb.max_seqlen)
         assert st == fa.FA_OK
         assert fa.fa_device_status() == fa.FA_OK
@@ -127,7 +140,7 @@ def test_gather_bit_exact(fa):
         got = out.cpu().view(torch.int16).numpy()
         bt = pb.block_table.cpu().numpy()
         for b, L in enumerate(lens):
-            ref = oracle.gather_paged_kv(host, bt[b], L, 16)
+            ref = oracle.gather_paged_kv(host, bt[b], L, page_size)
             assert np.array_equal(got[b, :L], ref), f"seq {b}"
 
 
