@@ -390,8 +390,10 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
         const long long pool_rows = static_cast<long long>(num_pages) * page_size;
         CUtensorMap tq, tk, tv;
         if ((st = make_map(&tq, q, d, 1, static_cast<long long>(B) * H)) != FA_OK) return st;
-        if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, page_size)) != FA_OK) return st;
-        if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, page_size)) != FA_OK) return st;
+        // one box per page, or per 64-key block of a larger page
+        const int box_rows = page_size < fa::kDecodeTcBlock ? page_size : fa::kDecodeTcBlock;
+        if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, box_rows)) != FA_OK) return st;
+        if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, box_rows)) != FA_OK) return st;
         const int T = fa::kDecodeTcSplitTokens;
         const int splits = max_seqlen > T ? (max_seqlen + T - 1) / T : 1;
         const size_t slots = static_cast<size_t>(B) * H * splits;

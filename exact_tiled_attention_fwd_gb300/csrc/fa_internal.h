@@ -167,6 +167,7 @@ inline int decode_split_tokens(int /*max_seqlen*/) { return 512; }
 // so the partials fit the same workspace).
 constexpr int kDecodeTcMinGroup = 8;
 constexpr int kDecodeTcSplitTokens = 2048;
+constexpr int kDecodeTcBlock = 64;  // keys per K/V block of the tensor-core decode
 inline int decode_max_splits(int max_seqlen) {
     const int t = decode_split_tokens(max_seqlen);
     const int s = (max_seqlen + t - 1) / t;

@@ -16,7 +16,7 @@
 // and at the end O / l and lse = m + ln l (online softmax, same page §2.2).
 // The two tiles share every K/V load.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads; DECODE has warps 0-7 only):
 //   warp 0       TMA producer: both Q tiles once, then the K/V ring
 //   warp 1       allocates tensor memory; issues tile 0's tcgen05.mma
 //   warp 2       issues tile 1's tcgen05.mma
@@ -70,8 +70,9 @@
 //   DECODE  (with PAGED) single-token decode for a large query group: the
 //           group's query heads are the query rows of tile 0, grid.x splits
 //           the keys, and the epilogue writes each split's unnormalised O and
-//           (m, l) for the decode combine kernel; tile 1 is unused and its
-//           shared memory goes to a deeper K/V ring.
+//           (m, l) for the decode combine kernel.  One tile, 64-key blocks,
+//           256 threads, half the shared memory and 256 TMEM columns, so two
+//           CTAs share an SM.
 // Dispatch order (cta_unit): non-causal CTAs run the Q blocks of a head
 // together; causal ones hand out the heaviest Q blocks first, at d = 128 in
 // groups of 8 heads so that few heads' K/V are live in L2 at once.  Dense
@@ -87,36 +88,47 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 384;
 constexpr int kTiles = 2;  // Q tiles per CTA
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kPBound = 256.0f;  // 2^kRescaleThreshold: the largest P the reference allows
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 64 bf16: a panel of a Q or P tile
 constexpr int kMaxSlots = 6;
 
-// DECODE (one query tile: a group of at most 128 heads) gives the second
-// tile's Q and P space to the K/V ring, which holds 5 tiles instead of 3 at
-// d = 128: decode streams each K/V tile past little work, so its speed is
-// set by the bytes in flight.
+// Threads per CTA: 4 control warps and 4 softmax warps per Q tile.  DECODE
+// has one tile, and two CTAs share an SM.
+__host__ __device__ constexpr int cta_threads(bool DECODE) { return DECODE ? 256 : 384; }
+__host__ __device__ constexpr int ctas_per_sm(bool DECODE) { return DECODE ? 2 : 1; }
+
+// Prefill: two Q tiles, 128-key K/V blocks, a 3-slot K/V ring at d = 128
+// (6 at d = 64), all 512 TMEM columns (S^0 | S^1 | O^0 | O^1), one CTA per
+// SM.  DECODE (one query tile: a group of at most 128 heads) streams each
+// K/V block past little work, so its speed is set by the bytes in flight
+// per SM: 64-key blocks, half the shared memory (Q, one P tile of 64 keys,
+// a ring of 16 KiB slots) and 256 TMEM columns (S | O), so that two CTAs
+// share an SM and one's waits overlap the other's loads.
 template <int D, bool DECODE>
 struct PrefillSmem {
-    static constexpr uint32_t kTile = kBlockM * D * 2;         // one Q, K or V tile
-    static constexpr uint32_t kPTile = kBlockM * kBlockN * 2;  // one P tile
-    static constexpr int kSmemTiles = DECODE ? 1 : kTiles;     // Q and P tiles held
-    static constexpr int kSlots = D == 128 ? (DECODE ? 5 : 3) : 6;  // K/V ring
-    static constexpr uint32_t kQ = 0;                           // + t * kTile
-    static constexpr uint32_t kP = kQ + kSmemTiles * kTile;     // + t * kPTile
-    static constexpr uint32_t kKV = kP + kSmemTiles * kPTile;   // + slot * kTile
-    static constexpr uint32_t kBar = kKV + kSlots * kTile;
+    static constexpr int kBN = DECODE ? 64 : kBlockN;           // keys per K/V block
+    static constexpr uint32_t kQTile = kBlockM * D * 2;         // one Q tile
+    static constexpr uint32_t kKVTile = kBN * D * 2;            // one K or V tile
+    static constexpr uint32_t kKVPanel = kBN * 128;             // one 64-column panel of it
+    static constexpr uint32_t kPTile = kBlockM * kBN * 2;       // one P tile
+    static constexpr int kSmemTiles = DECODE ? 1 : kTiles;      // Q and P tiles held
+    static constexpr int kSlots = D == 128 ? 3 : 6;             // K/V ring
+    static constexpr uint32_t kQ = 0;                           // + t * kQTile
+    static constexpr uint32_t kP = kQ + kSmemTiles * kQTile;    // + t * kPTile
+    static constexpr uint32_t kKV = kP + kSmemTiles * kPTile;   // + slot * kKVTile
+    static constexpr uint32_t kBar = kKV + kSlots * kKVTile;
     static constexpr uint32_t kNumBars = 40;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kUsed = kAbort + 4;
-    // Requested dynamic size: 1 KiB alignment slack, and at least 116 KiB so
-    // that a single CTA occupies an SM (each CTA takes all 512 TMEM columns).
-    static constexpr uint32_t kDyn = (kUsed + 1024) > 118784u ? (kUsed + 1024) : 118784u;
+    // Requested dynamic size: 1 KiB alignment slack; a prefill CTA asks for
+    // at least 116 KiB so that it has its SM (and the 512 TMEM columns) alone.
+    static constexpr uint32_t kDyn = DECODE ? kUsed + 1024 : ((kUsed + 1024) > 118784u ? (kUsed + 1024) : 118784u);
+    static constexpr uint32_t kTmemCols = DECODE ? 256 : 512;
+    static constexpr uint32_t kOCol = DECODE ? 128 : 256;       // O^t at kOCol + t * 128
 };
 
 enum BarId : uint32_t {
@@ -149,15 +161,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ int pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int pos_v(int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; }
 
-// Keys visible to some row of the tile [r0, r_last]: the number of K/V
-// blocks the tile needs (0 if the tile has no valid row or sees no key).
-template <bool CAUSAL>
+// Keys visible to some row of the tile [r0, r_last]: the number of BN-key
+// K/V blocks the tile needs (0 if the tile has no valid row or sees no key).
+template <bool CAUSAL, int BN>
 __device__ __forceinline__ int tile_blocks(int r0, int r_last, int Lk, int diag) {
     if (r_last < r0) return 0;
-    int n = (Lk + kBlockN - 1) / kBlockN;
+    int n = (Lk + BN - 1) / BN;
     if (CAUSAL) {
         const int max_key = r_last + diag;
-        n = max_key < 0 ? 0 : min(n, max_key / kBlockN + 1);
+        n = max_key < 0 ? 0 : min(n, max_key / BN + 1);
     }
     return n;
 }
@@ -194,13 +206,15 @@ __device__ __forceinline__ void cta_unit(int x, int y, int nblk, int nheads, int
 }
 
 template <int D, bool CAUSAL, bool PAGED, bool DECODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(cta_threads(DECODE), ctas_per_sm(DECODE))
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
     using L = PrefillSmem<D, DECODE>;
+    constexpr int kThreads = cta_threads(DECODE);
+    constexpr int kBN = L::kBN;
     constexpr int kPanels = D / 64;
     constexpr int kSlots = L::kSlots;
-    constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
+    constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBN, false);
     constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
 
     extern __shared__ uint8_t smem_raw[];
@@ -269,14 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
         r_last[t] = min(Lq, row0 + (t + 1) * kBlockM) - 1;
-        nb[t] = tile_blocks<CAUSAL>(row0 + t * kBlockM, r_last[t], Lk, diag);
+        nb[t] = tile_blocks<CAUSAL, kBN>(row0 + t * kBlockM, r_last[t], Lk, diag);
     }
     const int nmax = max(nb[0], nb[1]);
     // Paged keys whose last page is only partly used: the stale slots past Lk
     // are loaded with the page, and their V rows are zeroed before the last
     // P.V (P is 0 there, but 0 * a non-finite stale value would not be).
     const int page_rows = PAGED ? 1 << p.page_shift : 1;  // tokens per page
-    const bool v_tail = PAGED && (Lk & (page_rows - 1)) != 0 && nmax > 0 && (Lk - 1) / kBlockN == nmax - 1;
+    const bool v_tail = PAGED && (Lk & (page_rows - 1)) != 0 && nmax > 0 && (Lk - 1) / kBN == nmax - 1;
     const long long lse_base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
@@ -306,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
+        tmem_alloc(sbase + L::kTmemSlot, L::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -318,10 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Register split: 384 threads launch with 168 each (64,512 in all); the
     // producer/MMA warp group drops and the two softmax groups rise, keeping
     // the sum: 128*72 + 2*128*216 = 128*56 + 2*128*224 = 64,512.  (The pair
-    // per head dim is the one ptxas allocates without spilling.)
+    // per head dim is the one ptxas allocates without spilling.)  DECODE:
+    // 256 threads with 128 each (two CTAs per SM): 128*72 + 128*184 =
+    // 128*56 + 128*200 = 32,768.
+    constexpr uint32_t kRegsLaunch = DECODE ? 128 : 168;
     constexpr uint32_t kRegsLow = D == 128 ? 72 : 56;
-    constexpr uint32_t kRegsHigh = D == 128 ? 216 : 224;
-    static_assert(128 * kRegsLow + 256 * kRegsHigh <= 168 * kThreads, "register split exceeds the launch");
+    constexpr uint32_t kRegsHigh = DECODE ? 256 - kRegsLow : (D == 128 ? 216 : 224);
+    static_assert(kRegsLaunch * kThreads * ctas_per_sm(DECODE) <= 65536, "launch registers");
+    static_assert(128 * kRegsLow + (kThreads - 128) * kRegsHigh <= kRegsLaunch * kThreads,
+                  "register split exceeds the launch");
     if (warp < 4) {
         regs_dec<kRegsLow>();
         if (warp == 0) {
@@ -333,10 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int t = 0; t < kTiles; ++t) {
                     if (nb[t] == 0) continue;
-                    mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kTile);
+                    mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kQTile);
 #pragma unroll
                     for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + L::kQ + t * L::kTile + pn * kPanelBytes, &tm_q, bar(B_Q_FULL + t), pn * 64,
+                        tma_load_3d(sbase + L::kQ + t * L::kQTile + pn * kPanelBytes, &tm_q, bar(B_Q_FULL + t), pn * 64,
                                     h, q_start + row0 + t * kBlockM);
                 }
             }
@@ -374,12 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                abort_flag, p.err, lim);
                         }
                         if (!ok) return;
-                        mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kTile);
+                        mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kKVTile);
                         const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
 #pragma unroll
                         for (int pn = 0; pn < kPanels; ++pn)
-                            tma_load_3d(sbase + L::kKV + s * L::kTile + pn * kPanelBytes, map, bar(B_KV_FULL + s),
-                                        pn * 64, hk, k_start + j * kBlockN);
+                            tma_load_3d(sbase + L::kKV + s * L::kKVTile + pn * L::kKVPanel, map, bar(B_KV_FULL + s),
+                                        pn * 64, hk, k_start + j * kBN);
                         account(i, j);
                     };
                     load(pos_k(0), true, 0);
@@ -421,24 +440,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 // Paged K/V: the whole warp runs the loop (its waits are
                 // warp-uniform); lane 0 posts the slot's byte count and each
-                // lane issues one page box (page lane / kPanels, panel
-                // lane % kPanels), so one instruction issues a whole tile:
-                // 16 boxes at d = 128 with 16-token pages, 2 with 128-token
-                // pages.  A page past the sequence, or a bad table entry, is
-                // loaded from just past the pool: TMA fills zeros there (and
-                // still counts the bytes).
-                const int ppb = kBlockN >> p.page_shift;  // pages per 128-key block
-                const int pg = lane / kPanels;             // this lane's page of a block
-                const int pn = lane % kPanels;             // and panel
-                const bool boxes = lane < ppb * kPanels;
+                // lane issues one box (box lane / kPanels of the block, panel
+                // lane % kPanels), so one instruction issues a whole tile.  A
+                // box is one page, or the block's share of a page larger than
+                // the block (box_rows = min(page, kBN) rows, the tensor maps'
+                // box height): 16 boxes at d = 128 with 16-token pages and
+                // 128-key blocks, 2 with 128-token pages.  A page past the
+                // sequence, or a bad table entry, is loaded from just past the
+                // pool: TMA fills zeros there (and still counts the bytes).
+                const int box_rows = min(page_rows, kBN);
+                const int bpb = kBN / box_rows;             // boxes per block (each panel)
+                const int pg = lane / kPanels;              // this lane's box of a block
+                const int pn = lane % kPanels;              // and panel
+                const bool boxes = lane < bpb * kPanels;
                 const int* bt = bt_row;
                 // Table entries are fetched one block ahead of their use: the
                 // entries of blocks j and j + 1 are in flight at once, kept by
                 // block parity.
                 auto fetch = [&](int blk) {
-                    return (boxes && blk < nmax && blk * kBlockN + pg * page_rows < Lk)
-                               ? __ldg(bt + blk * ppb + pg)
-                               : -1;
+                    const int key0 = blk * kBN + pg * box_rows;  // first key of the box
+                    return (boxes && blk < nmax && key0 < Lk) ? __ldg(bt + (key0 >> p.page_shift)) : -1;
                 };
                 int ent0 = fetch(0), ent1 = fetch(1);
                 bool ok = true;
@@ -452,19 +473,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            p.err, lim);
                     }
                     if (!ok) return;
-                    if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kTile);
+                    if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), L::kKVTile);
                     __syncwarp();
                     if (boxes) {
                         const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
                         const int page = (j & 1) ? ent1 : ent0;
+                        const int key0 = j * kBN + pg * box_rows;
                         int row = p.num_pages << p.page_shift;
-                        if (j * kBlockN + pg * page_rows < Lk) {
+                        if (key0 < Lk) {
                             if (page >= 0 && page < p.num_pages)
-                                row = page << p.page_shift;
+                                row = (page << p.page_shift) + (key0 & (page_rows - 1));
                             else if (pn == 0 && is_k)
                                 atomicOr(p.err, FA_DEVERR_INDEX);
                         }
-                        tma_load_3d(sbase + L::kKV + s * L::kTile + pn * kPanelBytes + pg * page_rows * 128, map,
+                        tma_load_3d(sbase + L::kKV + s * L::kKVTile + pn * L::kKVPanel + pg * box_rows * 128, map,
                                     bar(B_KV_FULL + s), pn * 64, hk, row);
                     }
                     __syncwarp();
@@ -496,15 +518,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // last V tile once it has landed, then releases the last P.V.
                 const int i_last = pos_v(nmax - 1, nmax);
                 if (warp_wait(bar(B_KV_FULL + i_last % kSlots), (i_last / kSlots) & 1, abort_flag, p.err, lim)) {
-                    const int kb = (nmax - 1) * kBlockN;
+                    const int kb = (nmax - 1) * kBN;
                     const int r_lo = Lk - kb;
-                    const int r_hi = ((Lk + page_rows - 1) & ~(page_rows - 1)) - kb;
-                    const uint32_t base = sbase + L::kKV + (i_last % kSlots) * L::kTile;
+                    const int r_hi = min(((Lk + page_rows - 1) & ~(page_rows - 1)) - kb, kBN);
+                    const uint32_t base = sbase + L::kKV + (i_last % kSlots) * L::kKVTile;
                     for (int e = lane; e < (r_hi - r_lo) * kPanels * 8; e += 32) {
                         const int chunk = e & 7;
                         const int pn = (e >> 3) % kPanels;
                         const int r = r_lo + (e >> 3) / kPanels;
-                        st_shared_v4(base + pn * kPanelBytes + r * 128 + chunk * 16, 0u, 0u, 0u, 0u);
+                        st_shared_v4(base + pn * L::kKVPanel + r * 128 + chunk * 16, 0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -519,12 +541,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Descriptor bases; a k-step only moves the start address, which
                 // is the low field of the descriptor (addresses stay < 256 KiB, so
                 // the addition never carries out of it).
-                const uint64_t dq = sdesc_sw128(sbase + L::kQ + t * L::kTile, 16, 1024);
+                const uint64_t dq = sdesc_sw128(sbase + L::kQ + t * L::kQTile, 16, 1024);
                 const uint64_t dp = sdesc_sw128(sbase + L::kP + t * L::kPTile, 16, 1024);
                 const uint64_t dk = sdesc_sw128(sbase + L::kKV, 16, 1024);
-                const uint64_t dv = sdesc_sw128(sbase + L::kKV, kPanelBytes, 1024);
+                const uint64_t dv = sdesc_sw128(sbase + L::kKV, L::kKVPanel, 1024);
                 const uint32_t t_s = tmem + t * 128;
-                const uint32_t t_o = tmem + 256 + t * 128;
+                const uint32_t t_o = tmem + L::kOCol + t * 128;
                 bool ok = warp_wait(bar(B_Q_FULL + t), 0, abort_flag, p.err, lim);
                 auto wait_item = [&](int i) {
                     ok = ok && warp_wait(bar(B_KV_FULL + i % kSlots), (i / kSlots) & 1, abort_flag, p.err, lim);
@@ -532,12 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S^t_j = Q^t K_j^T into the S^t columns.
                 auto issue_s = [&](int j) {
                     const int s = pos_k(j) % kSlots;
-                    const uint64_t b0 = dk + ((s * L::kTile) >> 4);
+                    const uint64_t b0 = dk + ((s * L::kKVTile) >> 4);
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
-                            mma_ss(t_s, dq + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
+                            const uint32_t offa = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+                            const uint32_t offb = ((kk >> 2) * L::kKVPanel + (kk & 3) * 32) >> 4;
+                            mma_ss(t_s, dq + offa, b0 + offb, kIdescS, kk > 0 ? 1u : 0u);
                         }
                         tc_commit(bar(B_S_FULL + t));
                         tc_commit(bar(B_KV_EMPTY + t * kMaxSlots + s));
@@ -547,10 +570,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O^t += P^t_j V_j, P from shared memory.
                 auto issue_pv = [&](int j) {
                     const int s = pos_v(j, nmax) % kSlots;
-                    const uint64_t b0 = dv + ((s * L::kTile) >> 4);
+                    const uint64_t b0 = dv + ((s * L::kKVTile) >> 4);
                     if (elect_one()) {
 #pragma unroll
-                        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
                             const uint32_t offp = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
                             mma_ss(t_o, dp + offp, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                         }
@@ -593,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cta_sync(kThreads);
         if (warp == 1) {
             tc_fence_after();
-            tmem_dealloc(tmem, kTmemCols);
+            tmem_dealloc(tmem, L::kTmemCols);
         }
         return;
     } else {
@@ -608,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_other = t == 0 ? nb[1] : nb[0];  // blocks of the other tile
         const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t s_col = t * 128;
-        const uint32_t o_col = 256 + t * 128;
+        const uint32_t o_col = L::kOCol + t * 128;
         // this row of the P tile (128-byte swizzle: chunk c of a 128-byte
         // panel row lands at (c ^ (row % 8)) * 16)
         const uint32_t p_row = sbase + L::kP + t * L::kPTile + r * 128;
@@ -623,19 +646,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t u[kBlockN];
-            tmem_ld128(t_row + s_col, u);
+            uint32_t u[kBN];
+            if constexpr (kBN == 128)
+                tmem_ld128(t_row + s_col, u);
+            else
+                tmem_ld64(t_row + s_col, u);
             // S^t_j is in registers: the issuer may overwrite its columns.
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_S_FREE + t));
-            const int kbase = j * kBlockN;
-            const bool need_mask = (kbase + kBlockN > Lk) || (CAUSAL && kbase + kBlockN - 1 > r0 + diag);
+            const int kbase = j * kBN;
+            const bool need_mask = (kbase + kBN > Lk) || (CAUSAL && kbase + kBN - 1 > r0 + diag);
             if (need_mask) {
                 int lim_c = Lk - 1 - kbase;
                 if (CAUSAL) lim_c = min(lim_c, row + diag - kbase);
 #pragma unroll
-                for (int i = 0; i < kBlockN; ++i)
+                for (int i = 0; i < kBN; ++i)
                     if (i > lim_c) u[i] = __float_as_uint(NEG_INF);
             }
             // The two tiles take turns on their exponentials (tile 1 block j
@@ -652,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P = 2^(S c - mu) as bf16 pairs and its row sum, kept in
             // registers until the P tile is free, so that the wait for the
             // previous P.V overlaps this work.
-            uint32_t pk[kBlockN / 2];
+            uint32_t pk[kBN / 2];
             float2 acc0, acc1;
             auto exponentials = [&](float mu) {
                 const float2 c2 = make_float2(c, c);
@@ -660,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc0 = make_float2(0.f, 0.f);
                 acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < kBlockN / 2; ++i) {
+                for (int i = 0; i < kBN / 2; ++i) {
                     const float2 x =
                         __ffma2_rn(make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2, nmu2);
                     const float2 e = make_float2(ex2(x.x), ex2(x.y));
@@ -687,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (exact) {
                 float mx0 = NEG_INF, mx1 = NEG_INF, mx2 = NEG_INF, mx3 = NEG_INF;
 #pragma unroll
-                for (int i = 0; i < kBlockN; i += 8) {
+                for (int i = 0; i < kBN; i += 8) {
                     mx0 = fmax3(mx0, __uint_as_float(u[i]), __uint_as_float(u[i + 1]));
                     mx1 = fmax3(mx1, __uint_as_float(u[i + 2]), __uint_as_float(u[i + 3]));
                     mx2 = fmax3(mx2, __uint_as_float(u[i + 4]), __uint_as_float(u[i + 5]));
@@ -724,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // keys 8c .. 8c+7 are 16-byte chunk c % 8 of panel c / 8
 #pragma unroll
-            for (int cc = 0; cc < kBlockN / 8; ++cc) {
+            for (int cc = 0; cc < kBN / 8; ++cc) {
                 const uint32_t addr = p_row + (cc >> 3) * kPanelBytes + ((static_cast<uint32_t>(cc & 7) ^ p_sw) << 4);
                 st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             }
@@ -789,6 +815,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                      cudaStream_t stream) {
     using L = PrefillSmem<D, DECODE>;
     static_assert(L::kDyn <= 232448u, "shared memory budget");
+    static_assert(!DECODE || 2 * (L::kDyn + 1024) <= 233472u, "two decode CTAs per SM");
     static_assert(L::kSlots <= kMaxSlots, "K/V ring");
     auto kern = prefill_kernel<D, CAUSAL, PAGED, DECODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
@@ -797,7 +824,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     const dim3 grid = DECODE    ? dim3(p.max_splits, 1, p.num_seqs)
                       : !CAUSAL ? dim3(nblk, p.H, p.num_seqs)
                                 : (D == 128 ? dim3(nblk * p.H, 1, p.num_seqs) : dim3(p.H, nblk, p.num_seqs));
-    kern<<<grid, kThreads, L::kDyn, stream>>>(tq, tk, tv, p);
+    kern<<<grid, cta_threads(DECODE), L::kDyn, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
