@@ -17,6 +17,13 @@ namespace fa {
 // Query rows per tile, keys per K/V block of the prefill kernel.
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
+// Keys per K/V block of the prefill kernel: 128, or 64 in its decode mode
+// (one Q tile, two CTAs per SM).  The host sizes every K/V tensor-map box
+// from this, so that no box is taller than the shared-memory slot it lands
+// in.
+__host__ __device__ constexpr bool small_shape(int /*D*/, bool decode) { return decode; }
+__host__ __device__ constexpr int kv_block_keys(int D, bool decode) { return small_shape(D, decode) ? 64 : kBlockN; }
+
 // Tokens per page of the paged KV cache: 16, 32, 64 or 128 (a power of two
 // that divides the 128-key block).  Kernels take it as a shift.  The
 // CUDA-core decode walks every page in chunks of kPageChunk tokens.
@@ -167,7 +174,6 @@ inline int decode_split_tokens(int /*max_seqlen*/) { return 512; }
 // so the partials fit the same workspace).
 constexpr int kDecodeTcMinGroup = 8;
 constexpr int kDecodeTcSplitTokens = 2048;
-constexpr int kDecodeTcBlock = 64;  // keys per K/V block of the tensor-core decode
 inline int decode_max_splits(int max_seqlen) {
     const int t = decode_split_tokens(max_seqlen);
     const int s = (max_seqlen + t - 1) / t;

@@ -97,8 +97,9 @@ constexpr int kMaxSlots = 6;
 
 // Threads per CTA: 4 control warps and 4 softmax warps per Q tile.  DECODE
 // has one tile, and two CTAs share an SM.
-__host__ __device__ constexpr int cta_threads(bool DECODE) { return DECODE ? 256 : 384; }
-__host__ __device__ constexpr int ctas_per_sm(bool DECODE) { return DECODE ? 2 : 1; }
+// small_shape() (fa_internal.h): one Q tile, 64-key blocks, two CTAs per SM.
+__host__ __device__ constexpr int cta_threads(bool SMALL) { return SMALL ? 256 : 384; }
+__host__ __device__ constexpr int ctas_per_sm(bool SMALL) { return SMALL ? 2 : 1; }
 
 // Prefill: two Q tiles, 128-key K/V blocks, a 3-slot K/V ring at d = 128
 // (6 at d = 64), all 512 TMEM columns (S^0 | S^1 | O^0 | O^1), one CTA per
@@ -107,7 +108,7 @@ __host__ __device__ constexpr int ctas_per_sm(bool DECODE) { return DECODE ? 2 :
 // per SM: 64-key blocks, half the shared memory (Q, one P tile of 64 keys,
 // a ring of 16 KiB slots) and 256 TMEM columns (S | O), so that two CTAs
 // share an SM and one's waits overlap the other's loads.
-template <int D, bool DECODE>
+template <int D, bool DECODE>  // DECODE: the small shape
 struct PrefillSmem {
     static constexpr int kBN = DECODE ? 64 : kBlockN;           // keys per K/V block
     static constexpr uint32_t kQTile = kBlockM * D * 2;         // one Q tile
@@ -206,11 +207,13 @@ __device__ __forceinline__ void cta_unit(int x, int y, int nblk, int nheads, int
 }
 
 template <int D, bool CAUSAL, bool PAGED, bool DECODE>
-__global__ void __launch_bounds__(cta_threads(DECODE), ctas_per_sm(DECODE))
+__global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_sm(small_shape(D, DECODE)))
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using L = PrefillSmem<D, DECODE>;
-    constexpr int kThreads = cta_threads(DECODE);
+    constexpr bool kSmall = small_shape(D, DECODE);
+    constexpr int kCtaTiles = kSmall ? 1 : kTiles;  // Q tiles this CTA computes
+    using L = PrefillSmem<D, kSmall>;
+    constexpr int kThreads = cta_threads(kSmall);
     constexpr int kBN = L::kBN;
     constexpr int kPanels = D / 64;
     constexpr int kSlots = L::kSlots;
@@ -228,7 +231,7 @@ __global__ void __launch_bounds__(cta_threads(DECODE), ctas_per_sm(DECODE))
     // Dispatch order: cta_unit above; grid.z is the sequence (with DECODE the
     // (sequence, kv head) pair, and grid.x the split of its keys).
     const int seq = blockIdx.z;
-    const int nblk = (p.num_q_blocks + 1) / 2;  // 256-row blocks
+    const int nblk = (p.num_q_blocks + kCtaTiles - 1) / kCtaTiles;  // Q blocks of kCtaTiles tiles
     int qb = 0, h = 0;
     if (!DECODE) cta_unit<D, CAUSAL>(static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y), nblk, p.H, qb, h);
     const int hk = DECODE ? seq % p.Hkv : h / p.group;
@@ -276,14 +279,14 @@ __global__ void __launch_bounds__(cta_threads(DECODE), ctas_per_sm(DECODE))
         k_start = seq * p.N;
         Lk = p.N;
     }
-    const int row0 = qb * kBlockM * kTiles;
+    const int row0 = qb * kBlockM * kCtaTiles;
     if (row0 >= Lq) return;
     const int diag = Lk - Lq;  // causal: key j visible to row i iff j <= i + diag
     int r_last[kTiles], nb[kTiles];
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
         r_last[t] = min(Lq, row0 + (t + 1) * kBlockM) - 1;
-        nb[t] = tile_blocks<CAUSAL, kBN>(row0 + t * kBlockM, r_last[t], Lk, diag);
+        nb[t] = t < kCtaTiles ? tile_blocks<CAUSAL, kBN>(row0 + t * kBlockM, r_last[t], Lk, diag) : 0;
     }
     const int nmax = max(nb[0], nb[1]);
     // Paged keys whose last page is only partly used: the stale slots past Lk
@@ -335,10 +338,10 @@ __global__ void __launch_bounds__(cta_threads(DECODE), ctas_per_sm(DECODE))
     // per head dim is the one ptxas allocates without spilling.)  DECODE:
     // 256 threads with 128 each (two CTAs per SM): 128*72 + 128*184 =
     // 128*56 + 128*200 = 32,768.
-    constexpr uint32_t kRegsLaunch = DECODE ? 128 : 168;
+    constexpr uint32_t kRegsLaunch = kSmall ? 128 : 168;
     constexpr uint32_t kRegsLow = D == 128 ? 72 : 56;
-    constexpr uint32_t kRegsHigh = DECODE ? 256 - kRegsLow : (D == 128 ? 216 : 224);
-    static_assert(kRegsLaunch * kThreads * ctas_per_sm(DECODE) <= 65536, "launch registers");
+    constexpr uint32_t kRegsHigh = kSmall ? 256 - kRegsLow : (D == 128 ? 216 : 224);
+    static_assert(kRegsLaunch * kThreads * ctas_per_sm(kSmall) <= 65536, "launch registers");
     static_assert(128 * kRegsLow + (kThreads - 128) * kRegsHigh <= kRegsLaunch * kThreads,
                   "register split exceeds the launch");
     if (warp < 4) {
@@ -424,8 +427,8 @@ __global__ void __launch_bounds__(cta_threads(DECODE), ctas_per_sm(DECODE))
                             cta_unit<D, CAUSAL>(bx, by, nblk, p.H, qb2, h2);
 #pragma unroll
                             for (int t = 0; t < kTiles; ++t) {
-                                const int rr = qb2 * kBlockM * kTiles + t * kBlockM;
-                                if (rr >= p.N) continue;
+                                const int rr = qb2 * kBlockM * kCtaTiles + t * kBlockM;
+                                if (t >= kCtaTiles || rr >= p.N) continue;
 #pragma unroll
                                 for (int pn = 0; pn < kPanels; ++pn)
                                     asm volatile(
@@ -813,18 +816,20 @@ __global__ void __launch_bounds__(cta_threads(DECODE), ctas_per_sm(DECODE))
 template <int D, bool CAUSAL, bool PAGED, bool DECODE = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      cudaStream_t stream) {
-    using L = PrefillSmem<D, DECODE>;
+    constexpr bool kSmall = small_shape(D, DECODE);
+    using L = PrefillSmem<D, kSmall>;
     static_assert(L::kDyn <= 232448u, "shared memory budget");
-    static_assert(!DECODE || 2 * (L::kDyn + 1024) <= 233472u, "two decode CTAs per SM");
+    static_assert(!kSmall || 2 * (L::kDyn + 1024) <= 233472u, "two CTAs per SM");
+    static_assert(L::kBN == kv_block_keys(D, DECODE), "the host sizes K/V boxes from kv_block_keys");
     static_assert(L::kSlots <= kMaxSlots, "K/V ring");
     auto kern = prefill_kernel<D, CAUSAL, PAGED, DECODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
     if (e != cudaSuccess) return e;
-    const int nblk = (p.num_q_blocks + 1) / 2;
+    const int nblk = (p.num_q_blocks + (kSmall ? 0 : 1)) / (kSmall ? 1 : 2);
     const dim3 grid = DECODE    ? dim3(p.max_splits, 1, p.num_seqs)
                       : !CAUSAL ? dim3(nblk, p.H, p.num_seqs)
                                 : (D == 128 ? dim3(nblk * p.H, 1, p.num_seqs) : dim3(p.H, nblk, p.num_seqs));
-    kern<<<grid, cta_threads(DECODE), L::kDyn, stream>>>(tq, tk, tv, p);
+    kern<<<grid, cta_threads(kSmall), L::kDyn, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
