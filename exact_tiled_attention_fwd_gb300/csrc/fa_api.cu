@@ -388,12 +388,12 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
     fa_status st = ensure_init(&err);
     if (st != FA_OK) return st;
     const int group = H / Hkv;
-    if (group >= fa::kDecodeTcMinGroup && group <= fa::kBlockM && static_cast<long long>(B) * Hkv <= 65535) {
+    if (group >= fa::kDecodeTcMinGroup && group <= fa::kDecodeQRows && static_cast<long long>(B) * Hkv <= 65535) {
         // Large query groups: the tensor-core decode (the group's query heads
         // are the rows of a Q tile), then the combine step.
         const long long pool_rows = static_cast<long long>(num_pages) * page_size;
         CUtensorMap tq, tk, tv;
-        if ((st = make_map(&tq, q, d, 1, static_cast<long long>(B) * H)) != FA_OK) return st;
+        if ((st = make_map(&tq, q, d, 1, static_cast<long long>(B) * H, fa::kDecodeQRows)) != FA_OK) return st;
         // one box per page, or per 64-key block of a larger page
         const int box_rows = page_size < fa::kv_block_keys(d, true) ? page_size : fa::kv_block_keys(d, true);
         if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, box_rows)) != FA_OK) return st;

@@ -173,6 +173,11 @@ inline int decode_split_tokens(int /*max_seqlen*/) { return 512; }
 // cores, in splits of kDecodeTcSplitTokens keys (a multiple of the 512 above,
 // so the partials fit the same workspace).
 constexpr int kDecodeTcMinGroup = 8;
+// The tensor-core decode loads the group's query heads as the first
+// kDecodeQRows rows of its query tile (the MMA reads 128 rows; the rows past
+// the group read neighbouring shared memory and are never stored), so groups
+// of up to this many heads decode there.
+constexpr int kDecodeQRows = 64;
 constexpr int kDecodeTcSplitTokens = 2048;
 inline int decode_max_splits(int max_seqlen) {
     const int t = decode_split_tokens(max_seqlen);

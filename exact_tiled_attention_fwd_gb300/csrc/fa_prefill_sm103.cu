@@ -111,12 +111,14 @@ __host__ __device__ constexpr int ctas_per_sm(bool SMALL) { return SMALL ? 2 : 1
 template <int D, bool DECODE>  // DECODE: the small shape
 struct PrefillSmem {
     static constexpr int kBN = DECODE ? 64 : kBlockN;           // keys per K/V block
-    static constexpr uint32_t kQTile = kBlockM * D * 2;         // one Q tile
+    static constexpr int kQRows = DECODE ? kDecodeQRows : kBlockM;  // Q rows loaded per tile
+    static constexpr uint32_t kQTile = kQRows * D * 2;          // one Q tile
+    static constexpr uint32_t kQPanel = kQRows * 128;           // one 64-column panel of it
     static constexpr uint32_t kKVTile = kBN * D * 2;            // one K or V tile
     static constexpr uint32_t kKVPanel = kBN * 128;             // one 64-column panel of it
     static constexpr uint32_t kPTile = kBlockM * kBN * 2;       // one P tile
     static constexpr int kSmemTiles = DECODE ? 1 : kTiles;      // Q and P tiles held
-    static constexpr int kSlots = D == 128 ? 3 : 6;             // K/V ring
+    static constexpr int kSlots = DECODE ? (D == 128 ? 4 : 6) : (D == 128 ? 3 : 6);  // K/V ring
     static constexpr uint32_t kQ = 0;                           // + t * kQTile
     static constexpr uint32_t kP = kQ + kSmemTiles * kQTile;    // + t * kPTile
     static constexpr uint32_t kKV = kP + kSmemTiles * kPTile;   // + slot * kKVTile
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
         }
         const int kbeg = split * p.split_tokens;
         if (kbeg >= L) return;
-        if (p.decode_group > kBlockM) {  // one query tile: the shared-memory layout holds no second
+        if (p.decode_group > L::kQRows) {  // the group's heads must fit the rows of the Q tile
             if (threadIdx.x == 0 && split == 0) atomicOr(p.err, FA_DEVERR_INDEX);
             return;
         }
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                     mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kQTile);
 #pragma unroll
                     for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + L::kQ + t * L::kQTile + pn * kPanelBytes, &tm_q, bar(B_Q_FULL + t), pn * 64,
+                        tma_load_3d(sbase + L::kQ + t * L::kQTile + pn * L::kQPanel, &tm_q, bar(B_Q_FULL + t), pn * 64,
                                     h, q_start + row0 + t * kBlockM);
                 }
             }
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t offa = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+                            const uint32_t offa = ((kk >> 2) * L::kQPanel + (kk & 3) * 32) >> 4;
                             const uint32_t offb = ((kk >> 2) * L::kKVPanel + (kk & 3) * 32) >> 4;
                             mma_ss(t_s, dq + offa, b0 + offb, kIdescS, kk > 0 ? 1u : 0u);
                         }
@@ -821,6 +823,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     static_assert(L::kDyn <= 232448u, "shared memory budget");
     static_assert(!kSmall || 2 * (L::kDyn + 1024) <= 233472u, "two CTAs per SM");
     static_assert(L::kBN == kv_block_keys(D, DECODE), "the host sizes K/V boxes from kv_block_keys");
+    static_assert(!DECODE || L::kQRows == kDecodeQRows, "the host sizes the decode Q box from kDecodeQRows");
     static_assert(L::kSlots <= kMaxSlots, "K/V ring");
     auto kern = prefill_kernel<D, CAUSAL, PAGED, DECODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));

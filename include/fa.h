@@ -209,10 +209,11 @@ size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen);
  * (num_pages + 1) * page_size must stay below 2^31.  causal is accepted;
  * under bottom-right alignment it does not change a single newest-token
  * query.
- * Groups of H / Hkv >= 8 query heads per kv head (up to 128) run on the
- * tensor cores: the group's query heads are the rows of one query tile, the
- * keys are taken in splits of 2048, and the splits are merged as in the
- * CUDA-core path.  Smaller groups use the CUDA-core split kernel.  The
+ * Groups of 8 to 64 query heads per kv head (H / Hkv) run on the tensor
+ * cores: the group's query heads are the rows of one query tile, the keys
+ * are taken in splits of 2048, and the splits are merged as in the
+ * CUDA-core path.  Smaller and larger groups use the CUDA-core split
+ * kernel.  The
  * results agree within the same tolerance; the workspace is the same.
  */
 int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache,

@@ -69,13 +69,14 @@ def test_gqa_decode(fa, H, Hkv, d):
 
 
 @pytest.mark.parametrize("H,Hkv,d", [(32, 4, 128), (32, 2, 64), (32, 1, 128), (128, 1, 64), (160, 1, 128),
-                                     (24, 2, 128), (48, 2, 64), (256, 1, 64), (320, 1, 64)])
+                                     (24, 2, 128), (48, 2, 64), (48, 1, 128), (64, 1, 128), (64, 1, 64),
+                                     (256, 1, 64), (320, 1, 64)])
 def test_tensor_core_decode(fa, H, Hkv, d):
-    """Groups of 8 to 128 query heads decode on the tensor cores (the
-    group's heads are the rows of a Q tile; groups of 12 and 24 leave it
-    part-used), in 2048-key splits merged by the combine step: empty,
-    one-token, page-edge and multi-split lengths.  Groups of 160, 256 and
-    320 fall back to the CUDA-core split kernel."""
+    """Groups of 8 to 64 query heads decode on the tensor cores (the
+    group's heads are the first rows of a Q tile; groups of 12, 24 and 48
+    leave it part-used), in 2048-key splits merged by the combine step:
+    empty, one-token, page-edge and multi-split lengths.  Groups of 128,
+    160, 256 and 320 take the CUDA-core split kernel."""
     check_full(fa, [0, 1, 15, 16, 17, 700, 2048, 2049, 4500], H, d, seed=30 + H + Hkv + d, Hkv=Hkv)
 
 
