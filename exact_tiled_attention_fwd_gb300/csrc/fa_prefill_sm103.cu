@@ -103,11 +103,13 @@ __host__ __device__ constexpr int ctas_per_sm(bool SMALL) { return SMALL ? 2 : 1
 
 // Prefill: two Q tiles, 128-key K/V blocks, a 3-slot K/V ring at d = 128
 // (6 at d = 64), all 512 TMEM columns (S^0 | S^1 | O^0 | O^1), one CTA per
-// SM.  DECODE (one query tile: a group of at most 128 heads) streams each
+// SM.  DECODE (one query tile: a group of at most 64 heads) streams each
 // K/V block past little work, so its speed is set by the bytes in flight
-// per SM: 64-key blocks, half the shared memory (Q, one P tile of 64 keys,
-// a ring of 16 KiB slots) and 256 TMEM columns (S | O), so that two CTAs
-// share an SM and one's waits overlap the other's loads.
+// per SM: 64-key blocks, half the shared memory (64 Q rows, one P tile of
+// 64 keys, a 4-slot ring of 16 KiB tiles) and 256 TMEM columns (S | O), so
+// that two CTAs share an SM and one's waits overlap the other's loads.  The
+// MMA reads 128 Q rows: rows 64-127 fall on the neighbouring shared memory
+// and give output rows that are never stored.
 template <int D, bool DECODE>  // DECODE: the small shape
 struct PrefillSmem {
     static constexpr int kBN = DECODE ? 64 : kBlockN;           // keys per K/V block
