@@ -355,12 +355,15 @@ int fa_store_kvcache(const void* k, const void* v, void* k_cache, void* v_cache,
 
 size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen) {
     if (B < 1 || H < 1 || max_seqlen < 0 || (d != 64 && d != 128)) return 0;
-    const size_t splits = static_cast<size_t>(fa::decode_max_splits(max_seqlen));
+    // The larger of the two paths' layouts: the tensor-core path keeps one
+    // more partial per (sequence, head) than the CUDA-core path's splits, and
+    // its plan (prefix[B + 1], seg_ns[B * Hkv <= B * H], W).
+    const size_t splits = static_cast<size_t>(fa::decode_max_splits(max_seqlen)) + 1;
     const size_t slots = static_cast<size_t>(B) * H * splits;
-    size_t bytes = slots * d * sizeof(float);
-    bytes = (bytes + 255) & ~size_t(255);
-    bytes += slots * 2 * sizeof(float);
-    return (bytes + 255) & ~size_t(255);
+    size_t bytes = (slots * d * sizeof(float) + 255) & ~size_t(255);
+    bytes += (slots * 2 * sizeof(float) + 255) & ~size_t(255);
+    bytes += ((static_cast<size_t>(B) + 1 + static_cast<size_t>(B) * H + 4) * sizeof(int) + 255) & ~size_t(255);
+    return bytes;
 }
 
 int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
@@ -388,7 +391,8 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
     fa_status st = ensure_init(&err);
     if (st != FA_OK) return st;
     const int group = H / Hkv;
-    if (group >= fa::kDecodeTcMinGroup && group <= fa::kDecodeQRows && static_cast<long long>(B) * Hkv <= 65535) {
+    if (group >= fa::kDecodeTcMinGroup && group <= fa::kDecodeQRows &&
+        static_cast<long long>(B) * Hkv * ((max_seqlen + 63) / 64) < (1ll << 31)) {
         // Large query groups: the tensor-core decode (the group's query heads
         // are the rows of a Q tile), then the combine step.
         const long long pool_rows = static_cast<long long>(num_pages) * page_size;
@@ -398,34 +402,39 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
         const int box_rows = page_size < fa::kv_block_keys(d, true) ? page_size : fa::kv_block_keys(d, true);
         if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, box_rows)) != FA_OK) return st;
         if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, box_rows)) != FA_OK) return st;
-        const int T = fa::kDecodeTcSplitTokens;
-        const int splits = max_seqlen > T ? (max_seqlen + T - 1) / T : 1;
+        // Partials: one more slot per (sequence, head) than the CUDA-core
+        // path's splits (a pair's blocks span at most that many CTAs), then
+        // the plan arrays.
+        const int splits = fa::decode_max_splits(max_seqlen) + 1;
         const size_t slots = static_cast<size_t>(B) * H * splits;
-        float* ws_o = static_cast<float*>(workspace);
-        float* ws_ml =
-            reinterpret_cast<float*>(static_cast<char*>(workspace) + ((slots * d * sizeof(float) + 255) & ~size_t(255)));
-        fa::PrefillParams pp{};
-        pp.num_seqs = B * Hkv;
-        pp.H = 1;
-        pp.Hkv = Hkv;
-        pp.group = 1;
-        pp.max_seqlen_q = group;
-        pp.max_seqlen_k = max_seqlen;
-        pp.total_q = B * H;
-        pp.num_q_blocks = (group + fa::kBlockM - 1) / fa::kBlockM;
-        pp.scale_log2 = scale * 1.4426950408889634f;
-        pp.err = err;
-        pp.wait_limit_ns = wait_limit_ns();
-        pp.block_table = block_table;
-        pp.max_pages = max_pages_per_seq;
-        pp.num_pages = num_pages;
-        pp.page_shift = fa::page_shift(page_size);
-        pp.seqlens = seqlens;
-        pp.decode_group = group;
-        pp.split_tokens = T;
-        pp.max_splits = splits;
-        pp.ws_o = ws_o;
-        pp.ws_ml = ws_ml;
+        char* w = static_cast<char*>(workspace);
+        float* ws_o = reinterpret_cast<float*>(w);
+        w += (slots * d * sizeof(float) + 255) & ~size_t(255);
+        float* ws_ml = reinterpret_cast<float*>(w);
+        w += (slots * 2 * sizeof(float) + 255) & ~size_t(255);
+        int* prefix = reinterpret_cast<int*>(w);
+        int* seg_ns = prefix + B + 1;
+        int* plan = seg_ns + static_cast<size_t>(B) * Hkv;
+        fa::DecodeTcParams tp{};
+        tp.seqlens = seqlens;
+        tp.block_table = block_table;
+        tp.ws_o = ws_o;
+        tp.ws_ml = ws_ml;
+        tp.prefix = prefix;
+        tp.seg_ns = seg_ns;
+        tp.plan = plan;
+        tp.err = err;
+        tp.B = B;
+        tp.H = H;
+        tp.Hkv = Hkv;
+        tp.group = group;
+        tp.max_pages = max_pages_per_seq;
+        tp.num_pages = num_pages;
+        tp.page_shift = fa::page_shift(page_size);
+        tp.max_seqlen = max_seqlen;
+        tp.max_splits = splits;
+        tp.scale_log2 = scale * 1.4426950408889634f;
+        tp.wait_limit_ns = wait_limit_ns();
         fa::DecodeParams p{};
         p.seqlens = seqlens;
         p.o = o;
@@ -437,15 +446,16 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
         p.num_pages = num_pages;
         p.max_pages = max_pages_per_seq;
         p.max_seqlen = max_seqlen;
-        p.split_tokens = T;
+        p.split_tokens = fa::decode_split_tokens(max_seqlen);
         p.max_splits = splits;
         p.page_shift = fa::page_shift(page_size);
         p.ws_o = ws_o;
         p.ws_ml = ws_ml;
-        p.scale_log2 = pp.scale_log2;
+        p.seg_ns = seg_ns;
+        p.scale_log2 = tp.scale_log2;
         p.err = err;
         cudaStream_t s = static_cast<cudaStream_t>(stream);
-        cudaError_t e = fa::launch_prefill(tq, tk, tv, pp, d, false, s);
+        cudaError_t e = fa::launch_decode_tc(tq, tk, tv, tp, d, s);
         if (e == cudaSuccess) e = fa::launch_decode_combine(p, d, s);
         return finish(e, s);
     }

@@ -112,6 +112,7 @@ __device__ __forceinline__ void axpy8(float (&o)[8], float p, const uint4& v) {
 // plain multi-head attention.
 template <int D, int G>
 __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(const DecodeParams p) {
+    grid_dependents_launch();  // the combine grid (its dependent) may queue behind this one
     constexpr int LPR = D / 8;         // lanes per key row
     constexpr int RPI = 32 / LPR;      // rows per warp load
     constexpr int NI = kPageChunk / RPI;  // loads per lane per chunk (K and V each)
@@ -367,6 +368,7 @@ __global__ void __launch_bounds__(split_warps<G>() * 32) decode_split_kernel(con
 
 template <int D>
 __global__ void __launch_bounds__(kDecodeWarps * 32) decode_combine_kernel(const DecodeParams p) {
+    grid_dependency_wait();  // the partials of the kernel ahead (launched as its dependent)
     constexpr int EPL = D / 32;  // elements per lane
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -374,7 +376,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_combine_kernel(const
     if (bh >= p.B * p.H) return;
     const int b = bh / p.H;
     const int L = clamp_seqlen(__ldg(p.seqlens + b), p.max_seqlen, p.err, false);
-    const int ns = (L + p.split_tokens - 1) / p.split_tokens;
+    const int ns = p.seg_ns != nullptr ? __ldg(p.seg_ns + b * p.Hkv + (bh % p.H) / p.group)
+                                       : (L + p.split_tokens - 1) / p.split_tokens;
     const size_t base = static_cast<size_t>(bh) * p.max_splits;
     float M = neg_inf();
     for (int s = 0; s < ns; ++s) M = fmaxf(M, p.ws_ml[(base + s) * 2]);
@@ -503,23 +506,25 @@ cudaError_t launch_split_grouped(const DecodeParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream) {
-    dim3 cgrid((p.B * p.H + kDecodeWarps - 1) / kDecodeWarps);
     cudaError_t e = d == 128 ? launch_split_grouped<128>(p, stream) : launch_split_grouped<64>(p, stream);
     if (e != cudaSuccess) return e;
-    if (d == 128)
-        decode_combine_kernel<128><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
-    else
-        decode_combine_kernel<64><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_decode_combine(p, d, stream);
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t stream) {
-    dim3 cgrid((p.B * p.H + kDecodeWarps - 1) / kDecodeWarps);
-    if (d == 128)
-        decode_combine_kernel<128><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
-    else
-        decode_combine_kernel<64><<<cgrid, kDecodeWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    // launched as the programmatic dependent of the split kernel: its launch
+    // overlaps that kernel's last CTAs, and it waits for the partials
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.B * p.H + kDecodeWarps - 1) / kDecodeWarps);
+    cfg.blockDim = dim3(kDecodeWarps * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (d == 128) return cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, p);
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, p);
 }
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {

@@ -79,6 +79,8 @@ struct DecodeParams {
     float* lse;              // fp32 [B, H], may be null
     float* ws_o;             // fp32 [B, H, max_splits, d] unnormalised partial O
     float* ws_ml;            // fp32 [B, H, max_splits, 2] partial (m, l), log2 domain
+    const int* seg_ns;       // partials per (b, kv head) when set (the tensor-core
+                             // decode's segments); else ceil(seqlens[b] / split_tokens)
     int B, H, Hkv, group;
     int num_pages, max_pages, max_seqlen;
     int split_tokens;        // tokens per split (multiple of kPageChunk)
@@ -87,6 +89,37 @@ struct DecodeParams {
     float scale_log2;
     unsigned int* err;
 };
+
+// Grouped decode on the tensor cores, persistent, with the keys divided
+// evenly ("stream-K"): the work is the sequence of 64-key blocks of every
+// (sequence b, kv head) pair, b-major; decode_tc_plan_kernel writes prefix[b]
+// = Hkv * (blocks of sequences before b) (prefix[B] = all blocks), the
+// blocks per CTA W = plan[0], and per pair the number of CTAs its blocks fall
+// to, seg_ns[b * Hkv + kv head].  CTA c then takes blocks [c W, (c + 1) W):
+// each stretch of them within one pair is a segment, whose unnormalised O
+// and (m, l) go to slot (b * H + kv head * group + row) * max_splits + s,
+// s = c - (first CTA of the pair) (the DecodeParams layout), which the
+// combine kernel merges.  q is viewed as [B * H, 1, d] and the K/V tensor
+// maps as the pool [num_pages << page_shift, Hkv, d].
+struct DecodeTcParams {
+    const int* seqlens;      // int32 [B]
+    const int* block_table;  // int32 [B, max_pages]
+    float* ws_o;
+    float* ws_ml;
+    int* prefix;             // int32 [B + 1], written by the plan kernel
+    int* seg_ns;             // int32 [B * Hkv], written by the plan kernel
+    int* plan;               // int32 [1]: W
+    unsigned int* err;
+    int B, H, Hkv, group;
+    int max_pages, num_pages, page_shift, max_seqlen;
+    int max_splits;          // slots per (b, head): at least ceil(max blocks / kDecodeTcMinBlocks) + 1
+    int grid;                // CTAs of the decode launch
+    float scale_log2;
+    unsigned long long wait_limit_ns;
+};
+// Each CTA of the tensor-core decode takes at least this many 64-key blocks
+// (so a pair spans at most ceil(blocks / this) + 1 CTAs).
+constexpr int kDecodeTcMinBlocks = 8;
 
 struct GatherParams {
     const void* cache;
@@ -105,6 +138,8 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 // The combine step alone (after a split kernel that filled ws_o / ws_ml).
 cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t stream);
+cudaError_t launch_decode_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             DecodeTcParams p, int d, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* err, unsigned long long limit_ns, cudaStream_t stream);
 
@@ -170,15 +205,14 @@ cudaError_t static_scratch(void** ptr, size_t* bytes);
 // Decode split sizing shared by the workspace query and the launch.
 inline int decode_split_tokens(int /*max_seqlen*/) { return 512; }
 // Query groups of at least this many heads per kv head decode on the tensor
-// cores, in splits of kDecodeTcSplitTokens keys (a multiple of the 512 above,
-// so the partials fit the same workspace).
+// cores, over an even division of the keys (DecodeTcParams); their partials
+// take one more slot per (sequence, head) than these splits.
 constexpr int kDecodeTcMinGroup = 8;
 // The tensor-core decode loads the group's query heads as the first
 // kDecodeQRows rows of its query tile (the MMA reads 128 rows; the rows past
 // the group read neighbouring shared memory and are never stored), so groups
 // of up to this many heads decode there.
 constexpr int kDecodeQRows = 64;
-constexpr int kDecodeTcSplitTokens = 2048;
 inline int decode_max_splits(int max_seqlen) {
     const int t = decode_split_tokens(max_seqlen);
     const int s = (max_seqlen + t - 1) / t;

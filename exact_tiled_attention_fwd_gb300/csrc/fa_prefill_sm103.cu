@@ -104,12 +104,16 @@ __host__ __device__ constexpr int ctas_per_sm(bool SMALL) { return SMALL ? 2 : 1
 // Prefill: two Q tiles, 128-key K/V blocks, a 3-slot K/V ring at d = 128
 // (6 at d = 64), all 512 TMEM columns (S^0 | S^1 | O^0 | O^1), one CTA per
 // SM.  DECODE (one query tile: a group of at most 64 heads) streams each
-// K/V block past little work, so its speed is set by the bytes in flight
-// per SM: 64-key blocks, half the shared memory (64 Q rows, one P tile of
-// 64 keys, a 4-slot ring of 16 KiB tiles) and 256 TMEM columns (S | O), so
-// that two CTAs share an SM and one's waits overlap the other's loads.  The
-// MMA reads 128 Q rows: rows 64-127 fall on the neighbouring shared memory
-// and give output rows that are never stored.
+// K/V block past little work, so its speed is set by how fast one CTA
+// turns its blocks around: 64-key blocks, half the shared memory (64 Q rows,
+// two P buffers of 64 rows and 64 keys, a 4-slot ring of 16 KiB tiles) and
+// 256 TMEM columns (S_even | S_odd | O), so that two CTAs share an SM and
+// one's waits overlap the other's loads.  S and P are double-buffered by
+// block parity: the softmax of block j + 1 runs while P.V_j is in flight.
+// The MMAs read 128 rows of Q and of P: rows 64-127 fall on the neighbouring
+// shared memory (Q's on the next panel and the P buffers, P's on the next
+// buffer or the first ring slot) and give output rows that are never
+// stored; the softmax threads of those rows store no P.
 template <int D, bool DECODE>  // DECODE: the small shape
 struct PrefillSmem {
     static constexpr int kBN = DECODE ? 64 : kBlockN;           // keys per K/V block
@@ -118,12 +122,13 @@ struct PrefillSmem {
     static constexpr uint32_t kQPanel = kQRows * 128;           // one 64-column panel of it
     static constexpr uint32_t kKVTile = kBN * D * 2;            // one K or V tile
     static constexpr uint32_t kKVPanel = kBN * 128;             // one 64-column panel of it
-    static constexpr uint32_t kPTile = kBlockM * kBN * 2;       // one P tile
+    static constexpr uint32_t kPTile = kQRows * kBN * 2;        // one P tile (the rows stored)
     static constexpr int kSmemTiles = DECODE ? 1 : kTiles;      // Q and P tiles held
     static constexpr int kSlots = DECODE ? (D == 128 ? 4 : 6) : (D == 128 ? 3 : 6);  // K/V ring
     static constexpr uint32_t kQ = 0;                           // + t * kQTile
     static constexpr uint32_t kP = kQ + kSmemTiles * kQTile;    // + t * kPTile
-    static constexpr uint32_t kKV = kP + kSmemTiles * kPTile;   // + slot * kKVTile
+    static constexpr uint32_t kKV = kP + 2 * kPTile;            // + slot * kKVTile (P: one per tile, or
+                                                                //   DECODE's two buffers)
     static constexpr uint32_t kBar = kKV + kSlots * kKVTile;
     static constexpr uint32_t kNumBars = 40;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
@@ -558,38 +563,68 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                 auto wait_item = [&](int i) {
                     ok = ok && warp_wait(bar(B_KV_FULL + i % kSlots), (i / kSlots) & 1, abort_flag, p.err, lim);
                 };
-                // S^t_j = Q^t K_j^T into the S^t columns.
+                // S^t_j = Q^t K_j^T into the S^t columns (the small shape: S
+                // buffer j % 2, with its barriers at index j % 2).
                 auto issue_s = [&](int j) {
                     const int s = pos_k(j) % kSlots;
+                    const int bi = kSmall ? (j & 1) : t;
                     const uint64_t b0 = dk + ((s * L::kKVTile) >> 4);
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t offa = ((kk >> 2) * L::kQPanel + (kk & 3) * 32) >> 4;
                             const uint32_t offb = ((kk >> 2) * L::kKVPanel + (kk & 3) * 32) >> 4;
-                            mma_ss(t_s, dq + offa, b0 + offb, kIdescS, kk > 0 ? 1u : 0u);
+                            mma_ss(t_s + (kSmall ? (j & 1) * kBN : 0), dq + offa, b0 + offb, kIdescS, kk > 0 ? 1u : 0u);
                         }
-                        tc_commit(bar(B_S_FULL + t));
+                        tc_commit(bar(B_S_FULL + bi));
                         tc_commit(bar(B_KV_EMPTY + t * kMaxSlots + s));
                     }
                     __syncwarp();
                 };
-                // O^t += P^t_j V_j, P from shared memory.
+                // O^t += P^t_j V_j, P from shared memory (the small shape: P
+                // buffer j % 2).
                 auto issue_pv = [&](int j) {
                     const int s = pos_v(j, nmax) % kSlots;
+                    const int bi = kSmall ? (j & 1) : t;
                     const uint64_t b0 = dv + ((s * L::kKVTile) >> 4);
+                    const uint64_t dpj = kSmall ? dp + (((j & 1) * L::kPTile) >> 4) : dp;
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
                             const uint32_t offp = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
-                            mma_ss(t_o, dp + offp, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                            mma_ss(t_o, dpj + offp, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc_commit(bar(B_P_EMPTY + t));
+                        tc_commit(bar(B_P_EMPTY + bi));
                         tc_commit(bar(B_KV_EMPTY + t * kMaxSlots + s));
                         if (j == n_t - 1) tc_commit(bar(B_O_FINAL + t));
                     }
                     __syncwarp();
                 };
+                if constexpr (kSmall) {
+                    // Two S buffers: S_{j+2} is issued once the softmax has
+                    // read S_j, after P.V_j (K_{j+2} follows V_j in the ring).
+                    wait_item(pos_k(0));
+                    if (ok) issue_s(0);
+                    if (n_t > 1) {
+                        wait_item(pos_k(1));
+                        if (ok) issue_s(1);
+                    }
+                    for (int j = 0; ok && j < n_t; ++j) {
+                        ok = ok && warp_wait(bar(B_P_FULL + (j & 1)), (j >> 1) & 1, abort_flag, p.err, lim);
+                        wait_item(pos_v(j, nmax));
+                        if (PAGED && v_tail && j == nmax - 1)
+                            ok = ok && warp_wait(bar(B_V_TAIL), 0, abort_flag, p.err, lim);
+                        if (!ok) break;
+                        issue_pv(j);
+                        if (j + 2 < n_t) {
+                            ok = ok && warp_wait(bar(B_S_FREE + (j & 1)), (j >> 1) & 1, abort_flag, p.err, lim);
+                            wait_item(pos_k(j + 2));
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_s(j + 2);
+                        }
+                    }
+                } else {
                 wait_item(pos_k(0));
                 if (ok) issue_s(0);
                 for (int j = 0; ok && j < n_t; ++j) {
@@ -607,6 +642,7 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                         ok = ok && warp_wait(bar(B_V_TAIL), 0, abort_flag, p.err, lim);
                     if (!ok) break;
                     issue_pv(j);
+                }
                 }
                 // Every MMA of this warp has finished before tensor memory is
                 // released.
@@ -648,7 +684,11 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
         float l = 0.f;
         bool ok = n_t > 0;
         for (int j = 0; ok && j < n_t; ++j) {
-            if (!warp_wait(bar(B_S_FULL + t), j & 1, abort_flag, p.err, lim)) {
+            // the small shape's S and P buffers and their barriers go by block
+            // parity: index j % 2, phase j / 2
+            const int bi = kSmall ? (j & 1) : t;
+            const uint32_t ph = kSmall ? ((j >> 1) & 1) : (j & 1);
+            if (!warp_wait(bar(B_S_FULL + bi), ph, abort_flag, p.err, lim)) {
                 ok = false;
                 break;
             }
@@ -657,11 +697,11 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
             if constexpr (kBN == 128)
                 tmem_ld128(t_row + s_col, u);
             else
-                tmem_ld64(t_row + s_col, u);
+                tmem_ld64(t_row + s_col + (kSmall ? (j & 1) * kBN : 0), u);
             // S^t_j is in registers: the issuer may overwrite its columns.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_S_FREE + t));
+            if (lane == 0) mbar_arrive(bar(B_S_FREE + bi));
             const int kbase = j * kBN;
             const bool need_mask = (kbase + kBN > Lk) || (CAUSAL && kbase + kBN - 1 > r0 + diag);
             if (need_mask) {
@@ -736,14 +776,29 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
             l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_EXP_TURN + (t ^ 1)));
-            // PV^t_{j-1} must be done before the P tile is rewritten or O^t is
-            // rescaled.  (PV^t_{j-2} is known done: it was issued before
-            // S^t_j.)
-            if (j > 0 && !warp_wait(bar(B_P_EMPTY + t), (j - 1) & 1, abort_flag, p.err, lim)) {
-                ok = false;
-                break;
+            const bool any_resc = __any_sync(0xffffffffu, resc);
+            if constexpr (kSmall) {
+                // P buffer j % 2 was last read by P.V_{j-2}; a rescale of O
+                // needs P.V_{j-1} done as well.
+                if (j >= 2 && !warp_wait(bar(B_P_EMPTY + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, p.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                if (any_resc && j >= 1 &&
+                    !warp_wait(bar(B_P_EMPTY + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, p.err, lim)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                // PV^t_{j-1} must be done before the P tile is rewritten or
+                // O^t is rescaled.  (PV^t_{j-2} is known done: it was issued
+                // before S^t_j.)
+                if (j > 0 && !warp_wait(bar(B_P_EMPTY + t), (j - 1) & 1, abort_flag, p.err, lim)) {
+                    ok = false;
+                    break;
+                }
             }
-            if (__any_sync(0xffffffffu, resc)) {
+            if (any_resc) {
                 tc_fence_after();
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
@@ -755,16 +810,20 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                 }
                 tmem_st_wait();
             }
-            // keys 8c .. 8c+7 are 16-byte chunk c % 8 of panel c / 8
+            // keys 8c .. 8c+7 are 16-byte chunk c % 8 of panel c / 8 (the small
+            // shape's P tile holds rows 0 .. kQRows - 1 only)
+            if (!kSmall || r < L::kQRows) {
 #pragma unroll
-            for (int cc = 0; cc < kBN / 8; ++cc) {
-                const uint32_t addr = p_row + (cc >> 3) * kPanelBytes + ((static_cast<uint32_t>(cc & 7) ^ p_sw) << 4);
-                st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                for (int cc = 0; cc < kBN / 8; ++cc) {
+                    const uint32_t addr = p_row + (kSmall ? (j & 1) * L::kPTile : 0) + (cc >> 3) * kPanelBytes +
+                                          ((static_cast<uint32_t>(cc & 7) ^ p_sw) << 4);
+                    st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                }
             }
             // make the P rows visible to the tensor core, then publish
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL + t));
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + bi));
         }
         // ---- epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2; with DECODE
         // the split's unnormalised O and (m, l) for the combine step.

@@ -107,6 +107,16 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
     }
 }
 
+// ------------------------------------------------------------------ grid dependencies
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the kernel ahead of it in the stream has
+// finished; grid_dependency_wait() returns once that kernel has completed and
+// its writes are visible (at once when the launch had no such attribute).
+// grid_dependents_launch() lets the kernel behind this one start early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
@@ -121,6 +131,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// The same with an L2 cache policy (from l2_evict_first_policy, for data
+// read once).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, uint32_t bar, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+// An L2 policy that marks every line it covers evict-first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both

@@ -188,3 +188,31 @@ def test_deterministic(fa):
     o2, l2 = run_paged(fa, pb, 4, 128, 0.088)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d,page_size", [(128, 16), (64, 32), (128, 128)])
+def test_tensor_core_decode_many_items(fa, d, page_size):
+    """The tensor-core decode's CTAs (two per SM) each take many
+    (split, sequence, kv head) items from a counter: 420 sequences, most of
+    them one or two 64-key blocks with a partly used last page, empty ones
+    between them, and a few long enough for several splits, so items of every
+    size follow each other within a CTA.  Checked element by element against
+    the oracle; a second call on the same inputs gives the same bits, so the
+    counter starts from zero on every call."""
+    rng = np.random.default_rng(71 + d + page_size)
+    lens = [int(x) for x in rng.integers(0, 140, size=420)]
+    for i in range(0, 420, 37):
+        lens[i] = 0
+    lens[5], lens[200], lens[399] = 4200, 2049, 6000
+    H, Hkv = 32, 2
+    pb = W.paged_inputs(lens, H, d, 72 + d, "cuda", Hkv=Hkv, slack_pages=2, page_size=page_size)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_paged(fa, pb, H, d, scale)
+    o2, lse2 = run_paged(fa, pb, H, d, scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    assert torch.equal(o, o2) and torch.equal(torch.nan_to_num(lse, neginf=-1e30), torch.nan_to_num(lse2, neginf=-1e30))
+    O_ref, L_ref = oracle.attention_paged(f64(pb.q), f64(pb.k_cache), f64(pb.v_cache), pb.block_table.cpu().numpy(),
+                                          lens, page_size, scale, True)
+    assert_o_close(o, O_ref, f"many items d{d} page {page_size}")
+    assert_lse_close(lse, L_ref, f"many items d{d} page {page_size}")
