@@ -138,7 +138,7 @@ fa_status dense_impl(Operand q, Operand k, Operand v, void* o, float* lse, int B
     if (st != FA_OK) return st;
     CUtensorMap tq, tk, tv;
     if ((st = make_map(&tq, q.base, d, H, rows, fa::kBlockM, q.row_stride)) != FA_OK) return st;
-    const int kv_box = fa::kv_block_keys(d, false);
+    const int kv_box = fa::kBlockN;
     if ((st = make_map(&tk, k.base, d, Hkv, rows, kv_box, k.row_stride)) != FA_OK) return st;
     if ((st = make_map(&tv, v.base, d, Hkv, rows, kv_box, v.row_stride)) != FA_OK) return st;
     fa::PrefillParams p{};
@@ -184,7 +184,7 @@ fa_status varlen_impl(Operand q, Operand k, Operand v, void* o, float* lse, cons
     if (st != FA_OK) return st;
     CUtensorMap tq, tk, tv;
     if ((st = make_map(&tq, q.base, d, H, total_q, fa::kBlockM, q.row_stride)) != FA_OK) return st;
-    const int kv_box = fa::kv_block_keys(d, false);
+    const int kv_box = fa::kBlockN;
     if ((st = make_map(&tk, k.base, d, Hkv, total_k, kv_box, k.row_stride)) != FA_OK) return st;
     if ((st = make_map(&tv, v.base, d, Hkv, total_k, kv_box, v.row_stride)) != FA_OK) return st;
     fa::PrefillParams p{};
@@ -293,7 +293,7 @@ int fa_varlen_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
     CUtensorMap tq, tk, tv;
     if ((st = make_map(&tq, q, d, H, total_q)) != FA_OK) return st;
     // one box per page, or per block-sized share of a page taller than a block
-    const int kv_box = page_size < fa::kv_block_keys(d, false) ? page_size : fa::kv_block_keys(d, false);
+    const int kv_box = page_size < fa::kBlockN ? page_size : fa::kBlockN;
     if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, kv_box)) != FA_OK) return st;
     if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, kv_box)) != FA_OK) return st;
     fa::PrefillParams p{};
@@ -399,7 +399,7 @@ int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const 
         CUtensorMap tq, tk, tv;
         if ((st = make_map(&tq, q, d, 1, static_cast<long long>(B) * H, fa::kDecodeQRows)) != FA_OK) return st;
         // one box per page, or per 64-key block of a larger page
-        const int box_rows = page_size < fa::kv_block_keys(d, true) ? page_size : fa::kv_block_keys(d, true);
+        const int box_rows = page_size < fa::kDecodeBlockN ? page_size : fa::kDecodeBlockN;
         if ((st = make_map(&tk, k_cache, d, Hkv, pool_rows, box_rows)) != FA_OK) return st;
         if ((st = make_map(&tv, v_cache, d, Hkv, pool_rows, box_rows)) != FA_OK) return st;
         // Partials: one more slot per (sequence, head) than the CUDA-core

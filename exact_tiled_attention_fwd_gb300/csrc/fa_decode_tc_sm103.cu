@@ -54,7 +54,7 @@
 namespace fa {
 namespace {
 
-constexpr int kBN = 64;                // keys per K/V block
+constexpr int kBN = kDecodeBlockN;     // keys per K/V block (64)
 constexpr int kQRows = kDecodeQRows;   // query rows loaded per segment (64)
 constexpr int kThreads = 256;
 constexpr int kPlanThreads = 1024;

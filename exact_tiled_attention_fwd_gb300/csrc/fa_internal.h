@@ -17,12 +17,10 @@ namespace fa {
 // Query rows per tile, keys per K/V block of the prefill kernel.
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-// Keys per K/V block of the prefill kernel: 128, or 64 in its decode mode
-// (one Q tile, two CTAs per SM).  The host sizes every K/V tensor-map box
-// from this, so that no box is taller than the shared-memory slot it lands
-// in.
-__host__ __device__ constexpr bool small_shape(int /*D*/, bool decode) { return decode; }
-__host__ __device__ constexpr int kv_block_keys(int D, bool decode) { return small_shape(D, decode) ? 64 : kBlockN; }
+// Keys per K/V block of the tensor-core decode.  The host sizes every K/V
+// tensor-map box from kBlockN or this, so that no box is taller than the
+// shared-memory slot it lands in.
+constexpr int kDecodeBlockN = 64;
 
 // Tokens per page of the paged KV cache: 16, 32, 64 or 128 (a power of two
 // that divides the 128-key block).  Kernels take it as a shift.  The
@@ -56,17 +54,6 @@ struct PrefillParams {
     const int* block_table;
     int max_pages, num_pages;
     int page_shift;          // log2 of the page size
-    // Grouped decode on the tensor cores (decode_group > 0, with a page
-    // table): CTA (split, 0, s) takes the decode_group query heads of pair
-    // s = (b, kv head) = (s / Hkv, s % Hkv) as its query rows (q viewed as
-    // [B * H, 1, d]) and the keys [split * split_tokens, ...) of sequence b
-    // (seqlens[b] keys), and writes the split's unnormalised O and (m, l) to
-    // ws_o / ws_ml at slot (b * H + head) * max_splits + split, the layout of
-    // DecodeParams below; the combine kernel then merges the splits.
-    const int* seqlens;
-    int decode_group, split_tokens, max_splits;
-    float* ws_o;
-    float* ws_ml;
 };
 
 struct DecodeParams {

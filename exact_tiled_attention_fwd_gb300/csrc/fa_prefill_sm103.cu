@@ -16,7 +16,7 @@
 // and at the end O / l and lse = m + ln l (online softmax, same page §2.2).
 // The two tiles share every K/V load.
 //
-// Warp roles (384 threads; DECODE has warps 0-7 only):
+// Warp roles (384 threads):
 //   warp 0       TMA producer: both Q tiles once, then the K/V ring
 //   warp 1       allocates tensor memory; issues tile 0's tcgen05.mma
 //   warp 2       issues tile 1's tcgen05.mma
@@ -67,12 +67,6 @@
 //           page's rows (16 to 128) per page and panel, each lane one box, the
 //           table entries fetched a block ahead (prefill chunks that continue
 //           a cached prefix).
-//   DECODE  (with PAGED) single-token decode for a large query group: the
-//           group's query heads are the query rows of tile 0, grid.x splits
-//           the keys, and the epilogue writes each split's unnormalised O and
-//           (m, l) for the decode combine kernel.  One tile, 64-key blocks,
-//           256 threads, half the shared memory and 256 TMEM columns, so two
-//           CTAs share an SM.
 // Dispatch order (cta_unit): non-causal CTAs run the Q blocks of a head
 // together; causal ones hand out the heaviest Q blocks first, at d = 128 in
 // groups of 8 heads so that few heads' K/V are live in L2 at once.  Dense
@@ -95,40 +89,23 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 64 bf16: a panel of a Q or P tile
 constexpr int kMaxSlots = 6;
 
-// Threads per CTA: 4 control warps and 4 softmax warps per Q tile.  DECODE
-// has one tile, and two CTAs share an SM.
-// small_shape() (fa_internal.h): one Q tile, 64-key blocks, two CTAs per SM.
-__host__ __device__ constexpr int cta_threads(bool SMALL) { return SMALL ? 256 : 384; }
-__host__ __device__ constexpr int ctas_per_sm(bool SMALL) { return SMALL ? 2 : 1; }
+// Threads per CTA: 4 control warps and 4 softmax warps per Q tile.
+constexpr int kThreads = 128 + kTiles * 128;
 
-// Prefill: two Q tiles, 128-key K/V blocks, a 3-slot K/V ring at d = 128
-// (6 at d = 64), all 512 TMEM columns (S^0 | S^1 | O^0 | O^1), one CTA per
-// SM.  DECODE (one query tile: a group of at most 64 heads) streams each
-// K/V block past little work, so its speed is set by how fast one CTA
-// turns its blocks around: 64-key blocks, half the shared memory (64 Q rows,
-// two P buffers of 64 rows and 64 keys, a 4-slot ring of 16 KiB tiles) and
-// 256 TMEM columns (S_even | S_odd | O), so that two CTAs share an SM and
-// one's waits overlap the other's loads.  S and P are double-buffered by
-// block parity: the softmax of block j + 1 runs while P.V_j is in flight.
-// The MMAs read 128 rows of Q and of P: rows 64-127 fall on the neighbouring
-// shared memory (Q's on the next panel and the P buffers, P's on the next
-// buffer or the first ring slot) and give output rows that are never
-// stored; the softmax threads of those rows store no P.
-template <int D, bool DECODE>  // DECODE: the small shape
+// Two Q tiles, 128-key K/V blocks, a 3-slot K/V ring at d = 128 (6 at
+// d = 64), all 512 TMEM columns (S^0 | S^1 | O^0 | O^1), one CTA per SM.
+template <int D>
 struct PrefillSmem {
-    static constexpr int kBN = DECODE ? 64 : kBlockN;           // keys per K/V block
-    static constexpr int kQRows = DECODE ? kDecodeQRows : kBlockM;  // Q rows loaded per tile
-    static constexpr uint32_t kQTile = kQRows * D * 2;          // one Q tile
-    static constexpr uint32_t kQPanel = kQRows * 128;           // one 64-column panel of it
+    static constexpr int kBN = kBlockN;                         // keys per K/V block
+    static constexpr uint32_t kQTile = kBlockM * D * 2;         // one Q tile
+    static constexpr uint32_t kQPanel = kBlockM * 128;          // one 64-column panel of it
     static constexpr uint32_t kKVTile = kBN * D * 2;            // one K or V tile
     static constexpr uint32_t kKVPanel = kBN * 128;             // one 64-column panel of it
-    static constexpr uint32_t kPTile = kQRows * kBN * 2;        // one P tile (the rows stored)
-    static constexpr int kSmemTiles = DECODE ? 1 : kTiles;      // Q and P tiles held
-    static constexpr int kSlots = DECODE ? (D == 128 ? 4 : 6) : (D == 128 ? 3 : 6);  // K/V ring
+    static constexpr uint32_t kPTile = kBlockM * kBN * 2;       // one P tile
+    static constexpr int kSlots = D == 128 ? 3 : 6;             // K/V ring
     static constexpr uint32_t kQ = 0;                           // + t * kQTile
-    static constexpr uint32_t kP = kQ + kSmemTiles * kQTile;    // + t * kPTile
-    static constexpr uint32_t kKV = kP + 2 * kPTile;            // + slot * kKVTile (P: one per tile, or
-                                                                //   DECODE's two buffers)
+    static constexpr uint32_t kP = kQ + kTiles * kQTile;        // + t * kPTile
+    static constexpr uint32_t kKV = kP + kTiles * kPTile;       // + slot * kKVTile
     static constexpr uint32_t kBar = kKV + kSlots * kKVTile;
     static constexpr uint32_t kNumBars = 40;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
@@ -136,9 +113,9 @@ struct PrefillSmem {
     static constexpr uint32_t kUsed = kAbort + 4;
     // Requested dynamic size: 1 KiB alignment slack; a prefill CTA asks for
     // at least 116 KiB so that it has its SM (and the 512 TMEM columns) alone.
-    static constexpr uint32_t kDyn = DECODE ? kUsed + 1024 : ((kUsed + 1024) > 118784u ? (kUsed + 1024) : 118784u);
-    static constexpr uint32_t kTmemCols = DECODE ? 256 : 512;
-    static constexpr uint32_t kOCol = DECODE ? 128 : 256;       // O^t at kOCol + t * 128
+    static constexpr uint32_t kDyn = (kUsed + 1024) > 118784u ? (kUsed + 1024) : 118784u;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kOCol = 256;                      // O^t at kOCol + t * 128
 };
 
 enum BarId : uint32_t {
@@ -215,14 +192,11 @@ __device__ __forceinline__ void cta_unit(int x, int y, int nblk, int nheads, int
     h = grp * hg + rem % gs;
 }
 
-template <int D, bool CAUSAL, bool PAGED, bool DECODE>
-__global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_sm(small_shape(D, DECODE)))
+template <int D, bool CAUSAL, bool PAGED>
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    constexpr bool kSmall = small_shape(D, DECODE);
-    constexpr int kCtaTiles = kSmall ? 1 : kTiles;  // Q tiles this CTA computes
-    using L = PrefillSmem<D, kSmall>;
-    constexpr int kThreads = cta_threads(kSmall);
+    using L = PrefillSmem<D>;
     constexpr int kBN = L::kBN;
     constexpr int kPanels = D / 64;
     constexpr int kSlots = L::kSlots;
@@ -237,39 +211,17 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Dispatch order: cta_unit above; grid.z is the sequence (with DECODE the
-    // (sequence, kv head) pair, and grid.x the split of its keys).
+    // Dispatch order: cta_unit above; grid.z is the sequence.
     const int seq = blockIdx.z;
-    const int nblk = (p.num_q_blocks + kCtaTiles - 1) / kCtaTiles;  // Q blocks of kCtaTiles tiles
+    const int nblk = (p.num_q_blocks + kTiles - 1) / kTiles;  // Q blocks of kTiles tiles
     int qb = 0, h = 0;
-    if (!DECODE) cta_unit<D, CAUSAL>(static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y), nblk, p.H, qb, h);
-    const int hk = DECODE ? seq % p.Hkv : h / p.group;
+    cta_unit<D, CAUSAL>(static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y), nblk, p.H, qb, h);
+    const int hk = h / p.group;
 
     // ---- sequence geometry (uniform over the CTA)
     int q_start, Lq, k_start, Lk;
     const int* bt_row = PAGED ? p.block_table + static_cast<size_t>(seq) * p.max_pages : nullptr;
-    const int split = DECODE ? static_cast<int>(blockIdx.x) : 0;
-    if (DECODE) {
-        // The decode_group query heads of kv head hk of sequence b are the
-        // query rows; this split's keys are a sub-sequence of b's pages.
-        const int b = seq / p.Hkv;
-        int L = __ldg(p.seqlens + b);
-        if (L < 0 || L > p.max_seqlen_k) {  // clamped as the combine step does
-            if (threadIdx.x == 0 && split == 0 && hk == 0) atomicOr(p.err, FA_DEVERR_INDEX);
-            L = L < 0 ? 0 : p.max_seqlen_k;
-        }
-        const int kbeg = split * p.split_tokens;
-        if (kbeg >= L) return;
-        if (p.decode_group > L::kQRows) {  // the group's heads must fit the rows of the Q tile
-            if (threadIdx.x == 0 && split == 0) atomicOr(p.err, FA_DEVERR_INDEX);
-            return;
-        }
-        Lk = min(p.split_tokens, L - kbeg);
-        k_start = 0;
-        q_start = seq * p.decode_group;
-        Lq = p.decode_group;
-        bt_row = p.block_table + static_cast<size_t>(b) * p.max_pages + (kbeg >> p.page_shift);
-    } else if (p.cu_q != nullptr) {
+    if (p.cu_q != nullptr) {
         q_start = p.cu_q[seq];
         Lq = p.cu_q[seq + 1] - q_start;
         k_start = p.cu_k[seq];
@@ -288,14 +240,14 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
         k_start = seq * p.N;
         Lk = p.N;
     }
-    const int row0 = qb * kBlockM * kCtaTiles;
+    const int row0 = qb * kBlockM * kTiles;
     if (row0 >= Lq) return;
     const int diag = Lk - Lq;  // causal: key j visible to row i iff j <= i + diag
     int r_last[kTiles], nb[kTiles];
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
         r_last[t] = min(Lq, row0 + (t + 1) * kBlockM) - 1;
-        nb[t] = t < kCtaTiles ? tile_blocks<CAUSAL, kBN>(row0 + t * kBlockM, r_last[t], Lk, diag) : 0;
+        nb[t] = tile_blocks<CAUSAL, kBN>(row0 + t * kBlockM, r_last[t], Lk, diag);
     }
     const int nmax = max(nb[0], nb[1]);
     // Paged keys whose last page is only partly used: the stale slots past Lk
@@ -306,9 +258,8 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
     const long long lse_base = p.cu_q ? q_start : static_cast<long long>(seq) * p.H * p.N;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
-    // Rows of a tile that sees no key at all: O = 0, LSE = -inf.  (A decode
-    // split always has keys.)
-    if (!DECODE && warp >= 4) {
+    // Rows of a tile that sees no key at all: O = 0, LSE = -inf.
+    if (warp >= 4) {
         const int t = (warp - 4) >> 2;
         const int row = row0 + t * kBlockM + (warp & 3) * 32 + lane;
         if (nb[t] == 0 && row <= r_last[t]) {
@@ -344,13 +295,11 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
     // Register split: 384 threads launch with 168 each (64,512 in all); the
     // producer/MMA warp group drops and the two softmax groups rise, keeping
     // the sum: 128*72 + 2*128*216 = 128*56 + 2*128*224 = 64,512.  (The pair
-    // per head dim is the one ptxas allocates without spilling.)  DECODE:
-    // 256 threads with 128 each (two CTAs per SM): 128*72 + 128*184 =
-    // 128*56 + 128*200 = 32,768.
-    constexpr uint32_t kRegsLaunch = kSmall ? 128 : 168;
+    // per head dim is the one ptxas allocates without spilling.)
+    constexpr uint32_t kRegsLaunch = 168;
     constexpr uint32_t kRegsLow = D == 128 ? 72 : 56;
-    constexpr uint32_t kRegsHigh = kSmall ? 256 - kRegsLow : (D == 128 ? 216 : 224);
-    static_assert(kRegsLaunch * kThreads * ctas_per_sm(kSmall) <= 65536, "launch registers");
+    constexpr uint32_t kRegsHigh = D == 128 ? 216 : 224;
+    static_assert(kRegsLaunch * kThreads <= 65536, "launch registers");
     static_assert(128 * kRegsLow + (kThreads - 128) * kRegsHigh <= kRegsLaunch * kThreads,
                   "register split exceeds the launch");
     if (warp < 4) {
@@ -436,8 +385,8 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                             cta_unit<D, CAUSAL>(bx, by, nblk, p.H, qb2, h2);
 #pragma unroll
                             for (int t = 0; t < kTiles; ++t) {
-                                const int rr = qb2 * kBlockM * kCtaTiles + t * kBlockM;
-                                if (t >= kCtaTiles || rr >= p.N) continue;
+                                const int rr = qb2 * kBlockM * kTiles + t * kBlockM;
+                                if (rr >= p.N) continue;
 #pragma unroll
                                 for (int pn = 0; pn < kPanels; ++pn)
                                     asm volatile(
@@ -563,68 +512,38 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                 auto wait_item = [&](int i) {
                     ok = ok && warp_wait(bar(B_KV_FULL + i % kSlots), (i / kSlots) & 1, abort_flag, p.err, lim);
                 };
-                // S^t_j = Q^t K_j^T into the S^t columns (the small shape: S
-                // buffer j % 2, with its barriers at index j % 2).
+                // S^t_j = Q^t K_j^T into the S^t columns.
                 auto issue_s = [&](int j) {
                     const int s = pos_k(j) % kSlots;
-                    const int bi = kSmall ? (j & 1) : t;
                     const uint64_t b0 = dk + ((s * L::kKVTile) >> 4);
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t offa = ((kk >> 2) * L::kQPanel + (kk & 3) * 32) >> 4;
                             const uint32_t offb = ((kk >> 2) * L::kKVPanel + (kk & 3) * 32) >> 4;
-                            mma_ss(t_s + (kSmall ? (j & 1) * kBN : 0), dq + offa, b0 + offb, kIdescS, kk > 0 ? 1u : 0u);
+                            mma_ss(t_s, dq + offa, b0 + offb, kIdescS, kk > 0 ? 1u : 0u);
                         }
-                        tc_commit(bar(B_S_FULL + bi));
+                        tc_commit(bar(B_S_FULL + t));
                         tc_commit(bar(B_KV_EMPTY + t * kMaxSlots + s));
                     }
                     __syncwarp();
                 };
-                // O^t += P^t_j V_j, P from shared memory (the small shape: P
-                // buffer j % 2).
+                // O^t += P^t_j V_j, P from shared memory.
                 auto issue_pv = [&](int j) {
                     const int s = pos_v(j, nmax) % kSlots;
-                    const int bi = kSmall ? (j & 1) : t;
                     const uint64_t b0 = dv + ((s * L::kKVTile) >> 4);
-                    const uint64_t dpj = kSmall ? dp + (((j & 1) * L::kPTile) >> 4) : dp;
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
                             const uint32_t offp = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
-                            mma_ss(t_o, dpj + offp, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                            mma_ss(t_o, dp + offp, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc_commit(bar(B_P_EMPTY + bi));
+                        tc_commit(bar(B_P_EMPTY + t));
                         tc_commit(bar(B_KV_EMPTY + t * kMaxSlots + s));
                         if (j == n_t - 1) tc_commit(bar(B_O_FINAL + t));
                     }
                     __syncwarp();
                 };
-                if constexpr (kSmall) {
-                    // Two S buffers: S_{j+2} is issued once the softmax has
-                    // read S_j, after P.V_j (K_{j+2} follows V_j in the ring).
-                    wait_item(pos_k(0));
-                    if (ok) issue_s(0);
-                    if (n_t > 1) {
-                        wait_item(pos_k(1));
-                        if (ok) issue_s(1);
-                    }
-                    for (int j = 0; ok && j < n_t; ++j) {
-                        ok = ok && warp_wait(bar(B_P_FULL + (j & 1)), (j >> 1) & 1, abort_flag, p.err, lim);
-                        wait_item(pos_v(j, nmax));
-                        if (PAGED && v_tail && j == nmax - 1)
-                            ok = ok && warp_wait(bar(B_V_TAIL), 0, abort_flag, p.err, lim);
-                        if (!ok) break;
-                        issue_pv(j);
-                        if (j + 2 < n_t) {
-                            ok = ok && warp_wait(bar(B_S_FREE + (j & 1)), (j >> 1) & 1, abort_flag, p.err, lim);
-                            wait_item(pos_k(j + 2));
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_s(j + 2);
-                        }
-                    }
-                } else {
                 wait_item(pos_k(0));
                 if (ok) issue_s(0);
                 for (int j = 0; ok && j < n_t; ++j) {
@@ -642,7 +561,6 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                         ok = ok && warp_wait(bar(B_V_TAIL), 0, abort_flag, p.err, lim);
                     if (!ok) break;
                     issue_pv(j);
-                }
                 }
                 // Every MMA of this warp has finished before tensor memory is
                 // released.
@@ -684,11 +602,7 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
         float l = 0.f;
         bool ok = n_t > 0;
         for (int j = 0; ok && j < n_t; ++j) {
-            // the small shape's S and P buffers and their barriers go by block
-            // parity: index j % 2, phase j / 2
-            const int bi = kSmall ? (j & 1) : t;
-            const uint32_t ph = kSmall ? ((j >> 1) & 1) : (j & 1);
-            if (!warp_wait(bar(B_S_FULL + bi), ph, abort_flag, p.err, lim)) {
+            if (!warp_wait(bar(B_S_FULL + t), j & 1, abort_flag, p.err, lim)) {
                 ok = false;
                 break;
             }
@@ -697,11 +611,11 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
             if constexpr (kBN == 128)
                 tmem_ld128(t_row + s_col, u);
             else
-                tmem_ld64(t_row + s_col + (kSmall ? (j & 1) * kBN : 0), u);
+                tmem_ld64(t_row + s_col, u);
             // S^t_j is in registers: the issuer may overwrite its columns.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_S_FREE + bi));
+            if (lane == 0) mbar_arrive(bar(B_S_FREE + t));
             const int kbase = j * kBN;
             const bool need_mask = (kbase + kBN > Lk) || (CAUSAL && kbase + kBN - 1 > r0 + diag);
             if (need_mask) {
@@ -776,29 +690,14 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
             l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_EXP_TURN + (t ^ 1)));
-            const bool any_resc = __any_sync(0xffffffffu, resc);
-            if constexpr (kSmall) {
-                // P buffer j % 2 was last read by P.V_{j-2}; a rescale of O
-                // needs P.V_{j-1} done as well.
-                if (j >= 2 && !warp_wait(bar(B_P_EMPTY + (j & 1)), ((j - 2) >> 1) & 1, abort_flag, p.err, lim)) {
-                    ok = false;
-                    break;
-                }
-                if (any_resc && j >= 1 &&
-                    !warp_wait(bar(B_P_EMPTY + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, p.err, lim)) {
-                    ok = false;
-                    break;
-                }
-            } else {
-                // PV^t_{j-1} must be done before the P tile is rewritten or
-                // O^t is rescaled.  (PV^t_{j-2} is known done: it was issued
-                // before S^t_j.)
-                if (j > 0 && !warp_wait(bar(B_P_EMPTY + t), (j - 1) & 1, abort_flag, p.err, lim)) {
-                    ok = false;
-                    break;
-                }
+            // PV^t_{j-1} must be done before the P tile is rewritten or O^t is
+            // rescaled.  (PV^t_{j-2} is known done: it was issued before
+            // S^t_j.)
+            if (j > 0 && !warp_wait(bar(B_P_EMPTY + t), (j - 1) & 1, abort_flag, p.err, lim)) {
+                ok = false;
+                break;
             }
-            if (any_resc) {
+            if (__any_sync(0xffffffffu, resc)) {
                 tc_fence_after();
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
@@ -810,42 +709,20 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
                 }
                 tmem_st_wait();
             }
-            // keys 8c .. 8c+7 are 16-byte chunk c % 8 of panel c / 8 (the small
-            // shape's P tile holds rows 0 .. kQRows - 1 only)
-            if (!kSmall || r < L::kQRows) {
+            // keys 8c .. 8c+7 are 16-byte chunk c % 8 of panel c / 8
 #pragma unroll
-                for (int cc = 0; cc < kBN / 8; ++cc) {
-                    const uint32_t addr = p_row + (kSmall ? (j & 1) * L::kPTile : 0) + (cc >> 3) * kPanelBytes +
-                                          ((static_cast<uint32_t>(cc & 7) ^ p_sw) << 4);
-                    st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                }
+            for (int cc = 0; cc < kBN / 8; ++cc) {
+                const uint32_t addr = p_row + (cc >> 3) * kPanelBytes + ((static_cast<uint32_t>(cc & 7) ^ p_sw) << 4);
+                st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             }
             // make the P rows visible to the tensor core, then publish
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL + bi));
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + t));
         }
-        // ---- epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2; with DECODE
-        // the split's unnormalised O and (m, l) for the combine step.
+        // ---- epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
         if (ok) ok = warp_wait(bar(B_O_FINAL + t), 0, abort_flag, p.err, lim);
-        if (DECODE && ok) {
-            tc_fence_after();
-            const bool store = row <= r_last[t];
-            const size_t slot = (static_cast<size_t>(q_start) + row) * p.max_splits + split;
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D);
-#pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t o[32];
-                tmem_ld32(t_row + o_col + ch * 32, o);
-                if (store) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[ch * 8 + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                                                      __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
-                }
-            }
-            if (store) *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(l > 0.f ? m_ref : NEG_INF, l);
-        } else if (ok) {
+        if (ok) {
             tc_fence_after();
             const bool store = row <= r_last[t];
             const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
@@ -876,24 +753,20 @@ __global__ void __launch_bounds__(cta_threads(small_shape(D, DECODE)), ctas_per_
     cta_sync(kThreads);
 }
 
-template <int D, bool CAUSAL, bool PAGED, bool DECODE = false>
+template <int D, bool CAUSAL, bool PAGED>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      cudaStream_t stream) {
-    constexpr bool kSmall = small_shape(D, DECODE);
-    using L = PrefillSmem<D, kSmall>;
+    using L = PrefillSmem<D>;
     static_assert(L::kDyn <= 232448u, "shared memory budget");
-    static_assert(!kSmall || 2 * (L::kDyn + 1024) <= 233472u, "two CTAs per SM");
-    static_assert(L::kBN == kv_block_keys(D, DECODE), "the host sizes K/V boxes from kv_block_keys");
-    static_assert(!DECODE || L::kQRows == kDecodeQRows, "the host sizes the decode Q box from kDecodeQRows");
+    static_assert(L::kBN == kBlockN, "the host sizes K/V boxes from kBlockN");
     static_assert(L::kSlots <= kMaxSlots, "K/V ring");
-    auto kern = prefill_kernel<D, CAUSAL, PAGED, DECODE>;
+    auto kern = prefill_kernel<D, CAUSAL, PAGED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
     if (e != cudaSuccess) return e;
-    const int nblk = (p.num_q_blocks + (kSmall ? 0 : 1)) / (kSmall ? 1 : 2);
-    const dim3 grid = DECODE    ? dim3(p.max_splits, 1, p.num_seqs)
-                      : !CAUSAL ? dim3(nblk, p.H, p.num_seqs)
-                                : (D == 128 ? dim3(nblk * p.H, 1, p.num_seqs) : dim3(p.H, nblk, p.num_seqs));
-    kern<<<grid, cta_threads(kSmall), L::kDyn, stream>>>(tq, tk, tv, p);
+    const int nblk = (p.num_q_blocks + kTiles - 1) / kTiles;
+    const dim3 grid = !CAUSAL ? dim3(nblk, p.H, p.num_seqs)
+                              : (D == 128 ? dim3(nblk * p.H, 1, p.num_seqs) : dim3(p.H, nblk, p.num_seqs));
+    kern<<<grid, kThreads, L::kDyn, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -908,11 +781,6 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int d, bool causal, cudaStream_t stream) {
     const bool paged = p.block_table != nullptr;
-    if (p.decode_group > 0) {
-        if (!paged || causal) return cudaErrorInvalidValue;
-        return d == 128 ? launch_t<128, false, true, true>(tq, tk, tv, p, stream)
-                        : launch_t<64, false, true, true>(tq, tk, tv, p, stream);
-    }
     if (d == 128)
         return paged ? launch_d<128, true>(tq, tk, tv, p, causal, stream) : launch_d<128, false>(tq, tk, tv, p, causal, stream);
     return paged ? launch_d<64, true>(tq, tk, tv, p, causal, stream) : launch_d<64, false>(tq, tk, tv, p, causal, stream);
