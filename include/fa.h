@@ -184,7 +184,8 @@ int fa_store_kvcache(const void* k, const void* v, void* k_cache, void* v_cache,
 
 /*
  * Bytes of device workspace fa_paged_fwd needs for these sizes (the split-KV
- * partial results).  Returns 0 for invalid sizes.
+ * partial results and, for the tensor-core path, the plan of its work
+ * division).  Returns 0 for invalid sizes.
  */
 size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen);
 
@@ -210,11 +211,13 @@ size_t fa_paged_workspace_size(int B, int H, int d, int max_seqlen);
  * under bottom-right alignment it does not change a single newest-token
  * query.
  * Groups of 8 to 64 query heads per kv head (H / Hkv) run on the tensor
- * cores: the group's query heads are the rows of one query tile, the keys
- * are taken in splits of 2048, and the splits are merged as in the
- * CUDA-core path.  Smaller and larger groups use the CUDA-core split
- * kernel.  The
- * results agree within the same tolerance; the workspace is the same.
+ * cores: the group's query heads are the rows of one query tile, the
+ * 64-key blocks of all (sequence, kv head) pairs are divided evenly over
+ * two persistent CTAs per SM, and each CTA's partial results are merged as
+ * in the CUDA-core path (three kernels on `stream`: a plan of the division,
+ * the decode, the merge).  Smaller and larger groups use the CUDA-core split
+ * kernel and its merge.  The results agree within the same tolerance; the
+ * workspace is the same.
  */
 int fa_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
                  const int* block_table, const int* seqlens, void* o, float* lse,
