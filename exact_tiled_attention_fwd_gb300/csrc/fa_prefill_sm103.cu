@@ -116,6 +116,10 @@ struct PrefillSmem {
     static constexpr uint32_t kDyn = (kUsed + 1024) > 118784u ? (kUsed + 1024) : 118784u;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kOCol = 256;                      // O^t at kOCol + t * 128
+    // At d = 64, O^t uses 64 of its 128 columns and P^t (128 keys as bf16
+    // pairs) the other 64: the P.V product reads its A operand from TMEM.
+    static constexpr bool kPInTmem = D == 64;
+    static constexpr uint32_t kPColOff = 64;                    // P^t at O^t + kPColOff
 };
 
 enum BarId : uint32_t {
@@ -202,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kSlots = L::kSlots;
     constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBN, false);
     constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, true);
+    constexpr bool kPInTmem = L::kPInTmem;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -528,15 +533,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 };
-                // O^t += P^t_j V_j, P from shared memory.
+                // O^t += P^t_j V_j, P from shared memory, or at d = 64 from
+                // TMEM (keys 16 kk .. 16 kk + 15 are 8 columns at O^t + 64 + 8 kk).
                 auto issue_pv = [&](int j) {
                     const int s = pos_v(j, nmax) % kSlots;
                     const uint64_t b0 = dv + ((s * L::kKVTile) >> 4);
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
-                            const uint32_t offp = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
-                            mma_ss(t_o, dp + offp, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                            if constexpr (kPInTmem) {
+                                mma_ts(t_o, t_o + L::kPColOff + 8 * kk, b0 + ((kk * 16 * 128) >> 4), kIdescPV,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                            } else {
+                                const uint32_t offp = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+                                mma_ss(t_o, dp + offp, b0 + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                            }
                         }
                         tc_commit(bar(B_P_EMPTY + t));
                         tc_commit(bar(B_KV_EMPTY + t * kMaxSlots + s));
@@ -560,6 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (PAGED && v_tail && j == nmax - 1)
                         ok = ok && warp_wait(bar(B_V_TAIL), 0, abort_flag, p.err, lim);
                     if (!ok) break;
+                    tc_fence_after();  // P in TMEM (d = 64) was written by the softmax threads
                     issue_pv(j);
                 }
                 // Every MMA of this warp has finished before tensor memory is
@@ -709,14 +721,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
             }
-            // keys 8c .. 8c+7 are 16-byte chunk c % 8 of panel c / 8
+            if constexpr (kPInTmem) {
+                // P as bf16 pairs into the TMEM columns behind O^t
 #pragma unroll
-            for (int cc = 0; cc < kBN / 8; ++cc) {
-                const uint32_t addr = p_row + (cc >> 3) * kPanelBytes + ((static_cast<uint32_t>(cc & 7) ^ p_sw) << 4);
-                st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                for (int ch = 0; ch < kBN / 64; ++ch) {
+                    uint32_t part[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) part[i] = pk[32 * ch + i];
+                    tmem_st32(t_row + o_col + L::kPColOff + 32 * ch, part);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+            } else {
+                // keys 8c .. 8c+7 are 16-byte chunk c % 8 of panel c / 8
+#pragma unroll
+                for (int cc = 0; cc < kBN / 8; ++cc) {
+                    const uint32_t addr = p_row + (cc >> 3) * kPanelBytes + ((static_cast<uint32_t>(cc & 7) ^ p_sw) << 4);
+                    st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                }
+                // make the P rows visible to the tensor core
+                fence_proxy_async_smem();
             }
-            // make the P rows visible to the tensor core, then publish
-            fence_proxy_async_smem();
+            // publish
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_P_FULL + t));
         }
