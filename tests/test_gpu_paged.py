@@ -216,3 +216,16 @@ def test_tensor_core_decode_many_items(fa, d, page_size):
                                           lens, page_size, scale, True)
     assert_o_close(o, O_ref, f"many items d{d} page {page_size}")
     assert_lse_close(lse, L_ref, f"many items d{d} page {page_size}")
+
+
+def test_tensor_core_decode_large_batch(fa):
+    """2,500 sequences on the tensor-core decode: the plan kernel's 1024
+    threads each scan a run of three sequences' lengths (a path smaller
+    batches never take), with empty sequences at run boundaries and a few
+    long ones among many short ones."""
+    rng = np.random.default_rng(91)
+    lens = [int(x) for x in rng.integers(0, 70, size=2500)]
+    for i in (0, 1, 2, 3, 1023, 1024, 2047, 2048, 2499):
+        lens[i] = 0
+    lens[7], lens[1500], lens[2498] = 3000, 1100, 2049
+    check_full(fa, lens, 16, 128, seed=92, Hkv=1, slack=2, page_size=16)
