@@ -241,6 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = DkdvSmem<D>;
     constexpr int kPanels = D / 64;
     constexpr int kSlots = L::kSlots;
+    // The dQ kernel behind this one reads none of its results: it may start
+    // on the SMs this grid's last wave leaves free.
+    grid_dependents_launch();
     constexpr uint32_t kIdescT = idesc_bf16_f32(128, 128, false);  // S^T, dP^T
     constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, true);     // dV, dK
 
@@ -702,9 +705,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ib = CAUSAL ? (p.num_q_blocks - 1 - rank) : rank;
     const int hk = h / p.group;
     Geom g;
-    if (!seq_geom(p, seq, ib == 0 && h == 0 && threadIdx.x == 0, g)) return;
+    // This grid may start while the dK/dV grid ahead of it still runs (it
+    // reads none of dK/dV); every CTA waits for that grid before it exits, so
+    // that the work behind this one in the stream finds dK and dV written.
+    if (!seq_geom(p, seq, ib == 0 && h == 0 && threadIdx.x == 0, g)) {
+        grid_dependency_wait();
+        return;
+    }
     const int row0 = ib * kBlockM;
-    if (row0 >= g.Lq) return;
+    if (row0 >= g.Lq) {
+        grid_dependency_wait();
+        return;
+    }
     const int diag = g.Lk - g.Lq;
     const int r_last = min(g.Lq, row0 + kBlockM) - 1;
     int n_steps = (g.Lk + kBlockN - 1) / kBlockN;
@@ -727,6 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t off = (static_cast<size_t>(g.q_start + row0 + rr) * p.H + h) * D + cc * 8;
             *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + off) = make_uint4(0, 0, 0, 0);
         }
+        grid_dependency_wait();
         return;
     }
 
@@ -886,6 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             tmem_dealloc(tmem, kTmemCols);
         }
+        grid_dependency_wait();
         return;
     }
 
@@ -976,6 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     cta_sync(kThreads);
+    grid_dependency_wait();
 }
 
 // ============================================================== launch
@@ -997,12 +1012,22 @@ cudaError_t launch_dc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
+    // dQ needs only the prep kernel's lse2 / delta (complete before any dK/dV
+    // CTA ran), so it is launched to start in the dK/dV grid's tail.
     auto kb = bwd_dq_kernel<D, CAUSAL>;
     e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(DqSmem<D>::kDyn));
     if (e != cudaSuccess) return e;
-    const dim3 gb(p.num_q_blocks * p.H, 1, p.num_seqs);
-    kb<<<gb, kThreads, DqSmem<D>::kDyn, stream>>>(tq, tk, tv, tdo, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_q_blocks * p.H, 1, p.num_seqs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = DqSmem<D>::kDyn;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kb, tq, tk, tv, tdo, p);
 }
 
 }  // namespace
