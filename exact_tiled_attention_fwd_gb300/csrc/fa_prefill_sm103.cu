@@ -286,6 +286,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *abort_flag = 0;
         fence_barrier_init();
+        // The first loads need only the barriers: issue them now, so that they
+        // overlap the tensor-memory allocation and the CTA barrier.  The Q
+        // tiles, and with contiguous K/V the first K block (ring position 0,
+        // slot 0, which no tile has read before).
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) {
+            if (nb[t] == 0) continue;
+            mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kQTile);
+#pragma unroll
+            for (int pn = 0; pn < kPanels; ++pn)
+                tma_load_3d(sbase + L::kQ + t * L::kQTile + pn * L::kQPanel, &tm_q, bar(B_Q_FULL + t), pn * 64, h,
+                            q_start + row0 + t * kBlockM);
+        }
+        if constexpr (!PAGED) {
+            mbar_arrive_expect_tx(bar(B_KV_FULL + 0), L::kKVTile);
+#pragma unroll
+            for (int pn = 0; pn < kPanels; ++pn)
+                tma_load_3d(sbase + L::kKV + pn * L::kKVPanel, &tm_k, bar(B_KV_FULL + 0), pn * 64, hk, k_start);
+        }
     }
     if (warp == 1) {
         tmem_alloc(sbase + L::kTmemSlot, L::kTmemCols);
@@ -311,20 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         regs_dec<kRegsLow>();
         if (warp == 0) {
             // ================= TMA producer =================
-            if (lane == 0) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_k);
-                tma_prefetch_desc(&tm_v);
-#pragma unroll
-                for (int t = 0; t < kTiles; ++t) {
-                    if (nb[t] == 0) continue;
-                    mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kQTile);
-#pragma unroll
-                    for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + L::kQ + t * L::kQTile + pn * L::kQPanel, &tm_q, bar(B_Q_FULL + t), pn * 64,
-                                    h, q_start + row0 + t * kBlockM);
-                }
-            }
+            // (The Q tiles, and with contiguous K/V the first K block, were
+            // issued before the CTA barrier.)
             // Per (tile, slot): whether the tile reads the slot's current
             // occupant, and the parity of how many occupants it has read.
             uint32_t used = 0, par = 0;  // bit t * kMaxSlots + slot
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         pn * 64, hk, k_start + j * kBN);
                         account(i, j);
                     };
-                    load(pos_k(0), true, 0);
+                    account(pos_k(0), 0);  // K_0: issued before the CTA barrier
                     for (int j = 0; ok && j < nmax; ++j) {
                         if (j + 1 < nmax) load(pos_k(j + 1), true, j + 1);
                         load(pos_v(j, nmax), false, j);
