@@ -147,6 +147,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// 32 bytes to global memory in one instruction (the address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // Position of K_j / V_j in the load sequence K_0, K_1, V_0, K_2, V_1, ...,
 // K_{n-1}, V_{n-2}, V_{n-1} (n = blocks the CTA streams).
 __device__ __forceinline__ int pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
@@ -761,6 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             tc_fence_after();
             const bool store = row <= r_last[t];
+            const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;  // 32-byte stores
             const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
             uint16_t* orow = static_cast<uint16_t*>(p.o) + (static_cast<size_t>(q_start + row) * p.H + h) * D;
 #pragma unroll
@@ -772,9 +780,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
                 if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+                    if (o_v8) {
+                        // a row is D * 2 bytes, so every row start is 32-byte aligned too
+                        st_global_v8(orow + ch * 32, pk);
+                        st_global_v8(orow + ch * 32 + 16, pk + 8);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
                 }
             }
             if (store && p.lse != nullptr) {

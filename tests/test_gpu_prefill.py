@@ -168,3 +168,28 @@ def test_lse_optional_and_deterministic(fa):
     assert torch.equal(o1, o2), "two runs differ"
     o3, _ = fa.attention(q, k, v, scale=0.088, causal=True)
     assert torch.equal(o1, o3)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_16_byte_aligned(fa, d):
+    """An output buffer that starts 16 bytes past a 32-byte boundary (the
+    API's alignment floor) takes the 16-byte store path: the same values as
+    an aligned buffer, bit for bit, and the oracle's."""
+    B, N, H = 1, 300, 3
+    q, k, v = W.dense_inputs(B, N, H, d, 41, "cuda")
+    scale = 1.0 / np.sqrt(d)
+    o_al, lse_al = run_dense(fa, q, k, v, scale, True)
+    assert o_al.data_ptr() % 32 == 0
+    buf = torch.full((B * N * H * d + 8,), float("nan"), dtype=q.dtype, device=q.device)
+    o_off = buf[8:].view(B, N, H, d)  # 16 bytes past the allocation's (256-byte aligned) start
+    assert o_off.data_ptr() % 32 == 16
+    lse_off = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=q.device)
+    st = fa.fa_fwd(q, k, v, o_off, lse_off, B, H, H, N, d, scale, True)
+    assert st == fa.FA_OK, fa.status_string(st)
+    assert fa.fa_device_status() == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o_off, o_al)
+    assert torch.equal(lse_off, lse_al)
+    assert torch.isnan(buf[:8]).all(), "a store reached before the output"
+    O_ref, L_ref = oracle.attention_dense(f64(q), f64(k), f64(v), scale, True)
+    assert_o_close(o_off, O_ref, f"16-byte aligned o, d{d}")
