@@ -610,6 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t col = (which == 0 ? 256u : 384u) + half * (D / 2);
             const float mul = which == 0 ? 1.f : p.scale;
             uint16_t* dst = static_cast<uint16_t*>(which == 0 ? p.dv : p.dk) + off;
+            // 32-byte stores when the tensor is 32-byte aligned (a row share is
+            // D bytes, so every row share is then aligned too)
+            const bool v8 = (reinterpret_cast<uintptr_t>(which == 0 ? p.dv : p.dk) & 31u) == 0;
 #pragma unroll
             for (int ch = 0; ch < D / 64; ++ch) {
                 uint32_t v[32];
@@ -619,9 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
                 if (store) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+                    if (v8) {
+                        st_global_v8(dst + ch * 32, pk);
+                        st_global_v8(dst + ch * 32 + 16, pk + 8);
+                    } else {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
                 }
             }
         }
@@ -973,6 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool store = row <= r_last;
         uint16_t* dst = static_cast<uint16_t*>(p.dq) + (static_cast<size_t>(g.q_start + row) * p.H + h) * D +
                         half * (D / 2);
+        const bool v8 = (reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0;  // 32-byte stores
 #pragma unroll
         for (int ch = 0; ch < D / 64; ++ch) {
             uint32_t v[32];
@@ -982,9 +991,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i)
                 pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * p.scale, __uint_as_float(v[2 * i + 1]) * p.scale);
             if (store) {
-                uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+                if (v8) {
+                    st_global_v8(dst + ch * 32, pk);
+                    st_global_v8(dst + ch * 32 + 16, pk + 8);
+                } else {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
             }
         }
     }

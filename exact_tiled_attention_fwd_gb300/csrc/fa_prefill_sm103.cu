@@ -147,13 +147,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// 32 bytes to global memory in one instruction (the address 32-byte aligned).
-__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
 // Position of K_j / V_j in the load sequence K_0, K_1, V_0, K_2, V_1, ...,
 // K_{n-1}, V_{n-2}, V_{n-1} (n = blocks the CTA streams).
 __device__ __forceinline__ int pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }

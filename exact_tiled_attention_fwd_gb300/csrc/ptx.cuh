@@ -151,6 +151,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
+// 32 bytes to global memory in one instruction (the address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both
 // addresses 16-byte aligned), completion signalled as tx bytes on bar.
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

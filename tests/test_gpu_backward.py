@@ -138,6 +138,31 @@ def test_backward_deterministic(fa):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_outputs_16_byte_aligned(fa, d):
+    """dQ, dK and dV buffers 16 bytes past a 32-byte boundary (the API's
+    alignment floor) take the 16-byte store path: the same bits as aligned
+    buffers, and nothing written before them."""
+    B, N, H = 1, 300, 4
+    q, k, v = W.dense_inputs(B, N, H, d, 84, "cuda", Hkv=2)
+    do = W.randn_bf16((B, N, H, d), 85, "cuda")
+    o, lse = fa.attention(q, k, v, causal=True)
+    ref = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    bufs = [torch.full((x.numel() + 8,), float("nan"), dtype=x.dtype, device="cuda") for x in ref]
+    dq, dk, dv = (b[8:].view(x.shape) for b, x in zip(bufs, ref))
+    for x in (dq, dk, dv):
+        assert x.data_ptr() % 32 == 16
+    wsb = fa.fa_bwd_workspace_bytes(B, B * N, H)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    st = fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, wsb, B, H, 2, N, d, 1.0 / np.sqrt(d), 1)
+    assert st == fa.FA_OK, fa.status_string(st)
+    assert fa.fa_device_status() == fa.FA_OK
+    torch.cuda.synchronize()
+    for got, want, b in zip((dq, dk, dv), ref, bufs):
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+        assert torch.isnan(b[:8]).all(), "a store reached before the output"
+
+
 def test_backward_workspace_too_small(fa):
     B, N, H, d = 1, 64, 2, 64
     q, k, v = W.dense_inputs(B, N, H, d, 83, "cuda")
