@@ -291,23 +291,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < A_COUNT; ++i) mbar_init(bar(i), 1);
-        mbar_init(bar(A_S_FREE), 8);
-        mbar_init(bar(A_P_FULL), 8);
-        mbar_init(bar(A_DS_FULL), 8);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
-    const uint64_t lim = p.wait_limit_ns;
     // step n -> (query head, query block)
     auto step_head = [&](int n) { return hk * p.group + n / per_head; };
     // Each CTA starts its walk over the query blocks at its own offset (its
@@ -319,6 +302,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = n % per_head + rot;
         return i_lo + (m >= per_head ? m - per_head : m);
     };
+    const float* ws_seq = p.ws + bwd_ws_seq_offset(g.q_start, seq);  // this sequence's lse2 / delta rows
+    // Q_n (with lse2_n, delta_n) or dO_n into slot n % kSlots of its ring
+    auto load_step = [&](bool is_q, int n) {
+        const int s = n % kSlots;
+        const uint32_t full = (is_q ? A_Q_FULL : A_DO_FULL) + s;
+        const int hq = step_head(n), ib = step_block(n);
+        mbar_arrive_expect_tx(bar(full), L::kTile + (is_q ? 1024u : 0u));
+#pragma unroll
+        for (int pn = 0; pn < kPanels; ++pn)
+            tma_load_3d(sbase + (is_q ? L::kQR : L::kDR) + s * L::kTile + pn * kPanelBytes, is_q ? &tm_q : &tm_do,
+                        bar(full), pn * 64, hq, g.q_start + ib * kBlockM);
+        if (is_q) {
+            const float* src = ws_seq + hq * p.ws_head_stride + ib * kBlockM;
+            bulk_load_1d(sbase + L::kAuxR + s * L::kAux, src, 512, bar(full));
+            bulk_load_1d(sbase + L::kAuxR + s * L::kAux + 512, src + p.H * p.ws_head_stride, 512, bar(full));
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < A_COUNT; ++i) mbar_init(bar(i), 1);
+        mbar_init(bar(A_S_FREE), 8);
+        mbar_init(bar(A_P_FULL), 8);
+        mbar_init(bar(A_DS_FULL), 8);
+        *abort_flag = 0;
+        fence_barrier_init();
+        // The first loads need only the barriers: issue them now, so that they
+        // overlap the tensor-memory allocation and the CTA barrier.  K and V,
+        // then step 0's Q (with its lse2 / delta) and dO.
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+        mbar_arrive_expect_tx(bar(A_KV_FULL), 2 * L::kTile);
+#pragma unroll
+        for (int pn = 0; pn < kPanels; ++pn) {
+            tma_load_3d(sbase + L::kK + pn * kPanelBytes, &tm_k, bar(A_KV_FULL), pn * 64, hk, g.k_start + key0);
+            tma_load_3d(sbase + L::kV + pn * kPanelBytes, &tm_v, bar(A_KV_FULL), pn * 64, hk, g.k_start + key0);
+        }
+        load_step(true, 0);
+        load_step(false, 0);
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+    const uint64_t lim = p.wait_limit_ns;
 
     // 128 * 72 + 256 * 216 = 64,512 = 384 * 168 (the launch's registers).
     constexpr uint32_t kRegsLow = 72, kRegsHigh = 216;
@@ -332,39 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 const uint32_t ring_full = is_q ? A_Q_FULL : A_DO_FULL;
                 const uint32_t ring_empty = is_q ? A_Q_EMPTY : A_DO_EMPTY;
-                const uint32_t ring = is_q ? L::kQR : L::kDR;
-                const void* map = is_q ? static_cast<const void*>(&tm_q) : static_cast<const void*>(&tm_do);
-                tma_prefetch_desc(map);
-                if (is_q) {
-                    tma_prefetch_desc(&tm_k);
-                    tma_prefetch_desc(&tm_v);
-                    mbar_arrive_expect_tx(bar(A_KV_FULL), 2 * L::kTile);
-#pragma unroll
-                    for (int pn = 0; pn < kPanels; ++pn) {
-                        tma_load_3d(sbase + L::kK + pn * kPanelBytes, &tm_k, bar(A_KV_FULL), pn * 64, hk,
-                                    g.k_start + key0);
-                        tma_load_3d(sbase + L::kV + pn * kPanelBytes, &tm_v, bar(A_KV_FULL), pn * 64, hk,
-                                    g.k_start + key0);
-                    }
-                }
-                const float* ws_seq = p.ws + bwd_ws_seq_offset(g.q_start, seq);
                 bool ok = true;
-                for (int n = 0; ok && n < n_steps; ++n) {
+                // (K, V and step 0 were issued before the CTA barrier.)
+                for (int n = 1; ok && n < n_steps; ++n) {
                     const int s = n % kSlots;
                     if (n >= kSlots) ok = mbar_wait(bar(ring_empty + s), ((n / kSlots) - 1) & 1, abort_flag, p.err, lim);
                     if (!ok) break;
-                    const int hq = step_head(n), ib = step_block(n);
-                    mbar_arrive_expect_tx(bar(ring_full + s), L::kTile + (is_q ? 1024u : 0u));
-#pragma unroll
-                    for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + ring + s * L::kTile + pn * kPanelBytes, map, bar(ring_full + s), pn * 64,
-                                    hq, g.q_start + ib * kBlockM);
-                    if (is_q) {
-                        const float* src = ws_seq + hq * p.ws_head_stride + ib * kBlockM;
-                        bulk_load_1d(sbase + L::kAuxR + s * L::kAux, src, 512, bar(ring_full + s));
-                        bulk_load_1d(sbase + L::kAuxR + s * L::kAux + 512, src + p.H * p.ws_head_stride, 512,
-                                     bar(ring_full + s));
-                    }
+                    load_step(is_q, n);
                 }
                 // Drain: every copy this thread issued lands before the CTA exits.
                 if (is_q) mbar_wait_drain(bar(A_KV_FULL), 0, lim);
@@ -751,12 +758,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
+    // K_j or V_j into slot j % slots of its ring
+    auto load_kv = [&](bool is_k, int j) {
+        const int sl = j % (is_k ? kKS : kVS);
+        const uint32_t full = (is_k ? B_K_FULL : B_V_FULL) + sl;
+        mbar_arrive_expect_tx(bar(full), L::kTile);
+#pragma unroll
+        for (int pn = 0; pn < kPanels; ++pn)
+            tma_load_3d(sbase + (is_k ? L::kKR : L::kVR) + sl * L::kTile + pn * kPanelBytes, is_k ? &tm_k : &tm_v,
+                        bar(full), pn * 64, hk, g.k_start + kblock(j) * kBlockN);
+    };
+
     if (threadIdx.x == 0) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
         mbar_init(bar(B_DP_FREE), 8);
         mbar_init(bar(B_DS_FULL), 8);
         *abort_flag = 0;
         fence_barrier_init();
+        // The first loads need only the barriers: issue them now, so that they
+        // overlap the tensor-memory allocation and the CTA barrier.  Q and dO,
+        // then step 0's K and V.
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+        mbar_arrive_expect_tx(bar(B_QD_FULL), 2 * L::kTile);
+#pragma unroll
+        for (int pn = 0; pn < kPanels; ++pn) {
+            tma_load_3d(sbase + L::kQ + pn * kPanelBytes, &tm_q, bar(B_QD_FULL), pn * 64, h, g.q_start + row0);
+            tma_load_3d(sbase + L::kDO + pn * kPanelBytes, &tm_do, bar(B_QD_FULL), pn * 64, h, g.q_start + row0);
+        }
+        load_kv(true, 0);
+        load_kv(false, 0);
     }
     if (warp == 1) {
         tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
@@ -779,31 +812,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 const int nslots = is_k ? kKS : kVS;
                 const uint32_t full = is_k ? B_K_FULL : B_V_FULL, empty = is_k ? B_K_EMPTY : B_V_EMPTY;
-                const uint32_t ring = is_k ? L::kKR : L::kVR;
-                const void* map = is_k ? static_cast<const void*>(&tm_k) : static_cast<const void*>(&tm_v);
-                tma_prefetch_desc(map);
-                if (is_k) {
-                    tma_prefetch_desc(&tm_q);
-                    tma_prefetch_desc(&tm_do);
-                    mbar_arrive_expect_tx(bar(B_QD_FULL), 2 * L::kTile);
-#pragma unroll
-                    for (int pn = 0; pn < kPanels; ++pn) {
-                        tma_load_3d(sbase + L::kQ + pn * kPanelBytes, &tm_q, bar(B_QD_FULL), pn * 64, h,
-                                    g.q_start + row0);
-                        tma_load_3d(sbase + L::kDO + pn * kPanelBytes, &tm_do, bar(B_QD_FULL), pn * 64, h,
-                                    g.q_start + row0);
-                    }
-                }
                 bool ok = true;
-                for (int j = 0; ok && j < n_steps; ++j) {
+                // (Q, dO and step 0 were issued before the CTA barrier.)
+                for (int j = 1; ok && j < n_steps; ++j) {
                     const int sl = j % nslots;
                     if (j >= nslots) ok = mbar_wait(bar(empty + sl), ((j / nslots) - 1) & 1, abort_flag, p.err, lim);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar(full + sl), L::kTile);
-#pragma unroll
-                    for (int pn = 0; pn < kPanels; ++pn)
-                        tma_load_3d(sbase + ring + sl * L::kTile + pn * kPanelBytes, map, bar(full + sl), pn * 64, hk,
-                                    g.k_start + kblock(j) * kBlockN);
+                    load_kv(is_k, j);
                 }
                 // Drain: the last fill of every slot (and Q / dO).
                 if (is_k) mbar_wait_drain(bar(B_QD_FULL), 0, lim);
