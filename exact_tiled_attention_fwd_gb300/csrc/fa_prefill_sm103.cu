@@ -196,7 +196,7 @@ __device__ __forceinline__ void cta_unit(int x, int y, int nblk, int nheads, int
     h = grp * hg + rem % gs;
 }
 
-template <int D, bool CAUSAL, bool PAGED>
+template <int D, bool CAUSAL, bool PAGED, bool SLOTS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -216,11 +216,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Dispatch order: cta_unit above; grid.z is the sequence.
-    const int seq = blockIdx.z;
     const int nblk = (p.num_q_blocks + kTiles - 1) / kTiles;  // Q blocks of kTiles tiles
+    // Dispatch order: cta_unit above, grid.z the sequence; or, for a varlen
+    // grid that numbers its (sequence, block) slots (SLOTS), the slot (grid.y
+    // causal, grid.x otherwise) and the head (the other one).  Slots
+    // [B_s, B_{s+1}) belong to sequence s, B_s = s + floor(cu_q[s] / 256):
+    // at least ceil(Lq / 256) of them, sequence by sequence, so that no
+    // launch holds max_seqlen / 256 blocks for every sequence.
+    int seq = blockIdx.z;
     int qb = 0, h = 0;
-    cta_unit<D, CAUSAL>(static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y), nblk, p.H, qb, h);
+    int slot_rank = 0;  // slot grids: the slot's rank among its sequence's slots
+    if constexpr (SLOTS) {
+        const int y = static_cast<int>(CAUSAL ? blockIdx.y : blockIdx.x);
+        h = static_cast<int>(CAUSAL ? blockIdx.x : blockIdx.y);
+        const int t = threadIdx.x;  // sequence boundary t (the host keeps num_seqs < kThreads)
+        const int cq = t <= p.num_seqs ? p.cu_q[t] : 0;
+        seq = __syncthreads_count(t >= 1 && t <= p.num_seqs && t + cq / (kBlockM * kTiles) <= y);
+        if (blockIdx.x == 0 && blockIdx.y == 0 && t < p.num_seqs) {
+            // This CTA checks every sequence's offsets, since a sequence with
+            // bad ones may own no slot.
+            const int q0 = cq, lq = p.cu_q[t + 1] - cq, k0 = p.cu_k[t], lk = p.cu_k[t + 1] - k0;
+            if (q0 < 0 || lq < 0 || lk < 0 || q0 + lq > p.total_q || lq > p.max_seqlen_q || lk > p.max_seqlen_k ||
+                (PAGED ? lk > (static_cast<long long>(p.max_pages) << p.page_shift) : (k0 < 0 || k0 + lk > p.total_k)))
+                atomicOr(p.err, FA_DEVERR_INDEX);
+        }
+        if (seq >= p.num_seqs) return;  // past the last sequence's slots
+        slot_rank = y - (seq + p.cu_q[seq] / (kBlockM * kTiles));
+    } else {
+        cta_unit<D, CAUSAL>(static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y), nblk, p.H, qb, h);
+    }
     const int hk = h / p.group;
 
     // ---- sequence geometry (uniform over the CTA)
@@ -244,6 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         Lq = p.N;
         k_start = seq * p.N;
         Lk = p.N;
+    }
+    if constexpr (SLOTS) {
+        // the sequence's blocks in the slot order: the heaviest first under the
+        // causal mask, in order otherwise; slots past them stay empty
+        const int nb_seq = (Lq + kBlockM * kTiles - 1) / (kBlockM * kTiles);
+        if (slot_rank < 0 || slot_rank >= nb_seq) return;
+        qb = CAUSAL ? nb_seq - 1 - slot_rank : slot_rank;
     }
     const int row0 = qb * kBlockM * kTiles;
     if (row0 >= Lq) return;
@@ -803,8 +834,24 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     static_assert(L::kDyn <= 232448u, "shared memory budget");
     static_assert(L::kBN == kBlockN, "the host sizes K/V boxes from kBlockN");
     static_assert(L::kSlots <= kMaxSlots, "K/V ring");
-    auto kern = prefill_kernel<D, CAUSAL, PAGED>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
+    cudaError_t e;
+    // Contiguous varlen with fewer sequences than a CTA has threads: number
+    // the (sequence, block) slots (the causal d = 128 grid keeps its head
+    // groups).  A kernel of its own, so that the other launches keep their
+    // code.
+    if constexpr (!PAGED && (!CAUSAL || D == 64)) {
+        const long long slots = static_cast<long long>(p.num_seqs) + p.total_q / (kBlockM * kTiles);
+        if (p.cu_q != nullptr && p.num_seqs < kThreads && slots <= (CAUSAL ? 65535 : 2147483647ll)) {
+            auto ks = prefill_kernel<D, CAUSAL, PAGED, true>;
+            e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
+            if (e != cudaSuccess) return e;
+            const int n = static_cast<int>(slots);
+            ks<<<CAUSAL ? dim3(p.H, n, 1) : dim3(n, p.H, 1), kThreads, L::kDyn, stream>>>(tq, tk, tv, p);
+            return cudaGetLastError();
+        }
+    }
+    auto kern = prefill_kernel<D, CAUSAL, PAGED, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kDyn));
     if (e != cudaSuccess) return e;
     const int nblk = (p.num_q_blocks + kTiles - 1) / kTiles;
     const dim3 grid = !CAUSAL ? dim3(nblk, p.H, p.num_seqs)

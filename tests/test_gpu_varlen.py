@@ -136,3 +136,33 @@ def test_bad_cu_seqlens_reported(fa):
     assert st == fa.FA_OK
     assert fa.fa_device_status() == fa.FA_ERR_DEVICE_INDEX
     assert fa.fa_device_status() == fa.FA_OK  # cleared
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bad_sequence_without_slots_reported(fa, causal):
+    """Offsets [0, 300, 100, 310]: the middle sequence has a negative length,
+    so the launch's (sequence, block) slots give it none; it is still
+    reported, and the first sequence is still computed."""
+    lens = [300, 10]
+    q, k, v, cq, ck = W.varlen_inputs(lens, 2, 64, 17, "cuda")
+    bad = torch.tensor([0, 300, 100, 310], dtype=torch.int32, device="cuda")
+    o = torch.zeros_like(q)
+    st = fa.fa_varlen_fwd(q, k, v, o, None, bad, bad, 3, 512, 512, 310, 310, 2, 2, 64, 0.125, int(causal))
+    assert st == fa.FA_OK
+    assert fa.fa_device_status() == fa.FA_ERR_DEVICE_INDEX
+    assert fa.fa_device_status() == fa.FA_OK  # cleared
+    o_ref, _ = run_varlen(fa, q[:300], k[:300], v[:300], cq[:2], ck[:2], [300], [300], 0.125, causal)
+    torch.cuda.synchronize()
+    # rows 100.. are also the third sequence's (offsets 100..310), so only
+    # rows 0..99 are the first sequence's alone
+    assert torch.equal(o[:100], o_ref[:100]), "sequence 0 differs"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_sequences(fa, causal):
+    """400 sequences of 1 to 300 tokens: more sequences than a CTA has
+    threads, so the launch keeps one block per (sequence, Q block) of the
+    longest sequence."""
+    rng = np.random.default_rng(23)
+    lens = rng.integers(1, 301, size=400).tolist()
+    check_full(fa, lens, 2, 64, causal, seed=24)
