@@ -10,14 +10,18 @@
 //   S^t_j = Q^t K_j^T                    tcgen05.mma, SMEM x SMEM -> TMEM (fp32)
 //   m'    = max(m, rowmax(S^t_j scale))   softmax warps, one thread per row
 //   P^t_j = exp(S^t_j scale - m)          -> bf16 rows into shared memory
+//                                          (d = 128) or into TMEM behind O^t (d = 64)
 //   l     = l exp(m_old - m) + rowsum P^t_j
-//   O^t  += P^t_j V_j                     tcgen05.mma, SMEM x SMEM -> TMEM
+//   O^t  += P^t_j V_j                     tcgen05.mma, SMEM (or TMEM) x SMEM -> TMEM
 //
 // and at the end O / l and lse = m + ln l (online softmax, same page §2.2).
 // The two tiles share every K/V load.
 //
 // Warp roles (384 threads):
-//   warp 0       TMA producer: both Q tiles once, then the K/V ring
+//   warp 0       TMA producer: the K/V ring (its lane 0, thread 0, also
+//                initialises the barriers and issues both Q tiles and, with
+//                contiguous K/V, the first K block before the CTA barrier, so
+//                that those loads overlap the TMEM allocation)
 //   warp 1       allocates tensor memory; issues tile 0's tcgen05.mma
 //   warp 2       issues tile 1's tcgen05.mma
 //                (the whole warp runs the issue loop, with its waits and
@@ -32,11 +36,12 @@
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128) S^0   [128,256) S^1   [256,256+d) O^0   [384,384+d) O^1
+//   (d = 64: P^t as bf16 pairs in the 64 columns behind O^t)
 //
 // Decoupled S and P.  P^t_j goes to its own shared-memory tile (128 rows x
-// 128 keys, the K-major 128-byte-swizzled layout the MMA reads), not back
-// into tensor memory, so S^t's columns are free as soon as the softmax has
-// read them.  The softmax signals that right after its tensor-memory load,
+// 128 keys, the K-major 128-byte-swizzled layout the MMA reads) or, at
+// d = 64, to the TMEM columns behind O^t, never over S^t, so S^t's columns
+// are free as soon as the softmax has read them.  The softmax signals that right after its tensor-memory load,
 // and the issuer starts S^t_{j+1} while the softmax is still computing
 // P^t_j.  Per tile the issue order is S_0, S_1, PV_0, S_2, PV_1, ...; the
 // softmax warps of a tile therefore run block after block without waiting
@@ -62,11 +67,17 @@
 // past the sequence end are computed on whatever rows TMA brought in but
 // never stored.
 //
+// Epilogue: O^t / l to bf16, one row per thread, 32-byte stores when the
+// output is 32-byte aligned; LSE per row.
+//
 // Variants (template parameters):
 //   PAGED   K/V come through a page table: the producer issues one box of a
 //           page's rows (16 to 128) per page and panel, each lane one box, the
 //           table entries fetched a block ahead (prefill chunks that continue
 //           a cached prefix).
+//   SLOTS   contiguous varlen with fewer sequences than a CTA has threads:
+//           the grid numbers (sequence, 256-row block) slots instead of
+//           giving every sequence max_seqlen / 256 blocks (launch_t).
 // Dispatch order (cta_unit): non-causal CTAs run the Q blocks of a head
 // together; causal ones hand out the heaviest Q blocks first, at d = 128 in
 // groups of 8 heads so that few heads' K/V are live in L2 at once.  Dense
