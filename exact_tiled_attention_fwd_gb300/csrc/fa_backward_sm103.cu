@@ -25,7 +25,10 @@
 //   bwd_dq_kernel     one CTA per (128-row query block, head, sequence): Q_i
 //                     and dO_i stay in shared memory while the visible K/V
 //                     blocks stream past; dQ_i accumulates in tensor memory
-//                     and is written once
+//                     and is written once.  It reads none of dK/dV, so it is
+//                     launched to start in the dK/dV grid's tail
+//                     (programmatic dependent launch) and waits for that
+//                     grid only before its CTAs exit
 // dQ is therefore never accumulated with atomics across key blocks (the
 // article's §4.3 and §6.4 name those atomics as the cost to avoid, by
 // keeping the dQ accumulation on chip and writing it once); the price is
@@ -46,7 +49,9 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 idle, warps 4-11 compute
+// Warps 0 and 2: TMA producers (one operand ring each); warps 1 and 3: MMA
+// issuers (two issue streams); warps 4-11: compute.
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr float kLog2e = 1.4426950408889634f;
